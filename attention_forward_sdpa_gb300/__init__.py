@@ -1,0 +1,257 @@
+"""GB300 (sm_103a) fused scaled-dot-product-attention forward.
+
+Python face of the C ABI in include/attn_fwd.h (libattn_fwd_sm103.so).  This
+module only marshals arguments: it checks devices, dtypes and contiguity of
+torch tensors, passes raw pointers and sizes, and maps status codes to
+exceptions.  Every step of the computation runs in the library's CUDA
+kernels; there is no fallback of any kind.  If the library has not been built
+(``python -m attention_forward_sdpa_gb300.build_ext``) every call raises.
+
+Entry points (same names as the C functions):
+  attn_fwd_prefill, attn_fwd_decode, attn_decode_workspace_size,
+  attn_round_f32, attn_status_string, attn_abi_version
+and allocating conveniences ``prefill`` and ``decode`` that create the output
+(and the decode workspace) with torch on the inputs' device.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from .build_ext import LIB_PATH
+
+__all__ = ["attn_fwd_prefill", "attn_fwd_decode", "attn_decode_workspace_size",
+           "attn_round_f32", "attn_status_string", "attn_abi_version", "prefill", "decode",
+           "AttnError", "library_path", "load_library", "RTNE", "RTNA", "RTZ", "OUT_F32"]
+
+ATTN_OK = 0
+STATUS_NAMES = {0: "ATTN_OK", 1: "ATTN_ERR_INVALID_ARG", 2: "ATTN_ERR_UNSUPPORTED",
+                3: "ATTN_ERR_CUDA", 4: "ATTN_ERR_WORKSPACE", 5: "ATTN_ERR_BAD_BLOCK_TABLE",
+                6: "ATTN_ERR_TIMEOUT"}
+F16, BF16 = 0, 1
+RTNE, RTNA, RTZ, OUT_F32 = 0, 1, 2, 3
+
+_lock = threading.Lock()
+_lib = None
+
+
+class AttnError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = int(status)
+        super().__init__(f"{where}: {STATUS_NAMES.get(self.status, self.status)}")
+
+
+def library_path() -> str:
+    return LIB_PATH
+
+
+def load_library() -> ctypes.CDLL:
+    """Loads the built shared library; raises if it is missing."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"CUDA library not built: {LIB_PATH} is missing "
+                "(run `python -m attention_forward_sdpa_gb300.build_ext`)")
+        lib = ctypes.CDLL(LIB_PATH)
+        P, i32, i64, f32, sz = (ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float,
+                                ctypes.c_size_t)
+        lib.attn_fwd_prefill.restype = ctypes.c_int
+        lib.attn_fwd_prefill.argtypes = [P, P, P, P, P, i32, P, P, i32, i32, i32, i32, i32, i32,
+                                         i32, i32, i32, f32, i32, ctypes.c_int, ctypes.c_int, P,
+                                         P, P]
+        lib.attn_decode_workspace_size.restype = sz
+        lib.attn_decode_workspace_size.argtypes = [i32, i32, i32, i32]
+        lib.attn_fwd_decode.restype = ctypes.c_int
+        lib.attn_fwd_decode.argtypes = [P, P, P, P, P, i32, P, i32, i32, i32, i32, i32, i32, i32,
+                                        f32, i32, ctypes.c_int, ctypes.c_int, P, P, sz, P, P]
+        lib.attn_round_f32.restype = ctypes.c_int
+        lib.attn_round_f32.argtypes = [P, P, i64, ctypes.c_int, ctypes.c_int, P]
+        lib.attn_status_string.restype = ctypes.c_char_p
+        lib.attn_status_string.argtypes = [ctypes.c_int]
+        lib.attn_abi_version.restype = i32
+        lib.attn_abi_version.argtypes = []
+        _lib = lib
+        return lib
+
+
+# ----------------------------------------------------------------------------
+# marshalling helpers
+# ----------------------------------------------------------------------------
+
+def _dtype_code(t: torch.dtype) -> int:
+    if t == torch.bfloat16:
+        return BF16
+    if t == torch.float16:
+        return F16
+    raise TypeError(f"unsupported dtype {t}: expected torch.bfloat16 or torch.float16")
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _dev(t: torch.Tensor, name: str, dtype=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    return t
+
+
+def _stream_handle(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def _check(rc: int, where: str):
+    if rc != ATTN_OK:
+        raise AttnError(rc, where)
+
+
+# ----------------------------------------------------------------------------
+# C entry points
+# ----------------------------------------------------------------------------
+
+def attn_abi_version() -> int:
+    return int(load_library().attn_abi_version())
+
+
+def attn_status_string(status: int) -> str:
+    return load_library().attn_status_string(int(status)).decode()
+
+
+def attn_decode_workspace_size(num_seqs: int, num_q_heads: int, head_size: int,
+                               num_splits: int) -> int:
+    return int(load_library().attn_decode_workspace_size(num_seqs, num_q_heads, head_size,
+                                                         num_splits))
+
+
+def attn_fwd_prefill(out, q, k_cache, v_cache, block_table, query_start_loc, seq_lens, *,
+                     max_seqlen_q: int, max_seqlen_k: int, scale: float, causal: bool,
+                     rounding: int = RTNE, lse=None, status=None, stream=None) -> None:
+    """Calls attn_fwd_prefill on torch CUDA tensors (shapes as in the C header)."""
+    lib = load_library()
+    dt = _dtype_code(q.dtype)
+    _dev(q, "q")
+    _dev(k_cache, "k_cache", q.dtype)
+    _dev(v_cache, "v_cache", q.dtype)
+    _dev(out, "out", torch.float32 if rounding == OUT_F32 else q.dtype)
+    _dev(block_table, "block_table", torch.int32)
+    _dev(query_start_loc, "query_start_loc", torch.int32)
+    _dev(seq_lens, "seq_lens", torch.int32)
+    if lse is not None:
+        _dev(lse, "lse", torch.float32)
+    if status is not None:
+        _dev(status, "status", torch.int32)
+    total_q, hq, d = q.shape
+    nb, bs, hkv, d2 = k_cache.shape
+    if d2 != d or tuple(v_cache.shape) != tuple(k_cache.shape) or tuple(out.shape) != tuple(q.shape):
+        raise ValueError("inconsistent q / k_cache / v_cache / out shapes")
+    num_seqs = seq_lens.shape[0]
+    if query_start_loc.shape[0] != num_seqs + 1 or block_table.dim() != 2 or \
+            block_table.shape[0] != num_seqs:
+        raise ValueError("inconsistent query_start_loc / block_table / seq_lens shapes")
+    rc = lib.attn_fwd_prefill(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table),
+                              block_table.shape[1], _ptr(query_start_loc), _ptr(seq_lens),
+                              num_seqs, int(max_seqlen_q), int(max_seqlen_k), total_q, hq, hkv, d,
+                              bs, nb, float(scale), int(bool(causal)), dt, int(rounding),
+                              _ptr(lse), _ptr(status), _stream_handle(stream))
+    _check(rc, "attn_fwd_prefill")
+
+
+def attn_fwd_decode(out, q, k_cache, v_cache, block_table, seq_lens, *, max_seqlen_k: int,
+                    scale: float, num_splits: int, workspace=None, rounding: int = RTNE,
+                    lse=None, status=None, stream=None) -> None:
+    """Calls attn_fwd_decode on torch CUDA tensors (shapes as in the C header)."""
+    lib = load_library()
+    dt = _dtype_code(q.dtype)
+    _dev(q, "q")
+    _dev(k_cache, "k_cache", q.dtype)
+    _dev(v_cache, "v_cache", q.dtype)
+    _dev(out, "out", torch.float32 if rounding == OUT_F32 else q.dtype)
+    _dev(block_table, "block_table", torch.int32)
+    _dev(seq_lens, "seq_lens", torch.int32)
+    if lse is not None:
+        _dev(lse, "lse", torch.float32)
+    if status is not None:
+        _dev(status, "status", torch.int32)
+    ws_bytes = 0
+    if workspace is not None:
+        _dev(workspace, "workspace")
+        ws_bytes = workspace.numel() * workspace.element_size()
+    num_seqs, hq, d = q.shape
+    nb, bs, hkv, d2 = k_cache.shape
+    if d2 != d or tuple(v_cache.shape) != tuple(k_cache.shape) or tuple(out.shape) != tuple(q.shape):
+        raise ValueError("inconsistent q / k_cache / v_cache / out shapes")
+    if seq_lens.shape[0] != num_seqs or block_table.dim() != 2 or block_table.shape[0] != num_seqs:
+        raise ValueError("inconsistent block_table / seq_lens shapes")
+    rc = lib.attn_fwd_decode(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table),
+                             block_table.shape[1], _ptr(seq_lens), num_seqs, int(max_seqlen_k), hq,
+                             hkv, d, bs, nb, float(scale), int(num_splits), dt, int(rounding),
+                             _ptr(lse), _ptr(workspace), ws_bytes, _ptr(status),
+                             _stream_handle(stream))
+    _check(rc, "attn_fwd_decode")
+
+
+def attn_round_f32(out, x, *, dtype: torch.dtype, rounding: int, stream=None) -> None:
+    """Rounds fp32 CUDA tensor x into out (int16 tensor of the same size holding
+    bf16/fp16 bit patterns) with the epilogue's rounding."""
+    lib = load_library()
+    _dev(x, "x", torch.float32)
+    _dev(out, "out")
+    if out.element_size() != 2 or out.numel() != x.numel():
+        raise ValueError("out must be a 16-bit tensor with as many elements as x")
+    _check(lib.attn_round_f32(_ptr(out), _ptr(x), x.numel(), _dtype_code(dtype), int(rounding),
+                              _stream_handle(stream)), "attn_round_f32")
+
+
+# ----------------------------------------------------------------------------
+# allocating conveniences
+# ----------------------------------------------------------------------------
+
+def prefill(q, k_cache, v_cache, block_table, query_start_loc, seq_lens, *, max_seqlen_q: int,
+            max_seqlen_k: int, scale: float | None = None, causal: bool = True,
+            rounding: int = RTNE, return_lse: bool = False, status=None, stream=None):
+    """Returns O (and the log-sum-exp when asked) for a paged prefill problem."""
+    if scale is None:
+        scale = q.shape[-1] ** -0.5
+    out = torch.empty(q.shape, dtype=torch.float32 if rounding == OUT_F32 else q.dtype,
+                      device=q.device)
+    lse = torch.empty(q.shape[:2], dtype=torch.float32, device=q.device) if return_lse else None
+    attn_fwd_prefill(out, q, k_cache, v_cache, block_table, query_start_loc, seq_lens,
+                     max_seqlen_q=max_seqlen_q, max_seqlen_k=max_seqlen_k, scale=scale,
+                     causal=causal, rounding=rounding, lse=lse, status=status, stream=stream)
+    return (out, lse) if return_lse else out
+
+
+def decode(q, k_cache, v_cache, block_table, seq_lens, *, max_seqlen_k: int,
+           scale: float | None = None, num_splits: int = 8, rounding: int = RTNE,
+           return_lse: bool = False, workspace=None, status=None, stream=None):
+    """Returns O (and the log-sum-exp when asked) for one decode step."""
+    if scale is None:
+        scale = q.shape[-1] ** -0.5
+    out = torch.empty(q.shape, dtype=torch.float32 if rounding == OUT_F32 else q.dtype,
+                      device=q.device)
+    lse = torch.empty(q.shape[:2], dtype=torch.float32, device=q.device) if return_lse else None
+    if workspace is None:
+        n = attn_decode_workspace_size(q.shape[0], q.shape[1], q.shape[2], num_splits)
+        workspace = torch.empty(max(n, 16), dtype=torch.uint8, device=q.device) if n else None
+    attn_fwd_decode(out, q, k_cache, v_cache, block_table, seq_lens, max_seqlen_k=max_seqlen_k,
+                    scale=scale, num_splits=num_splits, workspace=workspace, rounding=rounding,
+                    lse=lse, status=status, stream=stream)
+    return (out, lse) if return_lse else out

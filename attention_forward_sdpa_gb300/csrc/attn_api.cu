@@ -1,0 +1,251 @@
+// attn_api.cu -- the extern "C" boundary declared in include/attn_fwd.h:
+// argument validation (all on the host, before any launch), device check,
+// TMA descriptor encoding and grid sizing.  Every compute step runs in the
+// kernels of prefill_tcgen05.cu and decode_splitkv.cu.
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/attn_fwd.h"
+#include "attn_internal.h"
+
+namespace {
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encode_fn() {
+  static std::once_flag once;
+  static EncodeTiledFn fn = nullptr;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  });
+  return fn;
+}
+
+// The kernels are built for sm_103a only.
+attn_status_t check_device() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ERR_CUDA;
+  int major = 0, minor = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  if (major != 10 || minor != 3) return ATTN_ERR_UNSUPPORTED;
+  return ATTN_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool encode(CUtensorMap* map, bool bf16, int rank, const cuuint64_t* dims,
+            const cuuint64_t* strides_bytes, const cuuint32_t* box, const void* base,
+            CUtensorMapSwizzle swz) {
+  EncodeTiledFn fn = get_encode_fn();
+  if (!fn) return false;
+  cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  return fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+            (cuuint32_t)rank, const_cast<void*>(base), dims, strides_bytes, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool valid_scale(float s) { return std::isfinite(s) && s > 0.f; }
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+}  // namespace
+
+extern "C" {
+
+int32_t attn_abi_version(void) { return 1; }
+
+const char* attn_status_string(attn_status_t s) {
+  switch (s) {
+    case ATTN_OK: return "ok";
+    case ATTN_ERR_INVALID_ARG: return "invalid argument";
+    case ATTN_ERR_UNSUPPORTED: return "unsupported configuration";
+    case ATTN_ERR_CUDA: return "CUDA error";
+    case ATTN_ERR_WORKSPACE: return "workspace missing, too small or misaligned";
+    case ATTN_ERR_BAD_BLOCK_TABLE: return "block table entry out of range";
+    case ATTN_ERR_TIMEOUT: return "pipeline wait timed out";
+  }
+  return "unknown status";
+}
+
+attn_status_t attn_fwd_prefill(void* out, const void* q, const void* k_cache, const void* v_cache,
+                               const int32_t* block_table, int32_t block_table_stride,
+                               const int32_t* query_start_loc, const int32_t* seq_lens,
+                               int32_t num_seqs, int32_t max_seqlen_q, int32_t max_seqlen_k,
+                               int32_t total_q, int32_t num_q_heads, int32_t num_kv_heads,
+                               int32_t head_size, int32_t block_size, int32_t num_blocks,
+                               float scale, int32_t causal, attn_dtype_t dtype,
+                               attn_round_t rounding, float* lse_out, int32_t* status_dev,
+                               void* stream) {
+  // ---- host-side validation (no CUDA call before this block ends)
+  if (num_seqs < 0 || max_seqlen_q < 0 || max_seqlen_k < 0 || total_q < 0) return ATTN_ERR_INVALID_ARG;
+  if (num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0) return ATTN_ERR_INVALID_ARG;
+  if (dtype != ATTN_F16 && dtype != ATTN_BF16) return ATTN_ERR_INVALID_ARG;
+  if (rounding < ATTN_RTNE || rounding > ATTN_OUT_F32) return ATTN_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return ATTN_ERR_INVALID_ARG;
+  if (!valid_scale(scale)) return ATTN_ERR_INVALID_ARG;
+  if (block_size <= 0 || num_blocks <= 0) return ATTN_ERR_INVALID_ARG;
+  if (head_size != 64 && head_size != 128) return ATTN_ERR_UNSUPPORTED;
+  if (block_size % 16 != 0 || !(128 % block_size == 0 || block_size % 128 == 0)) return ATTN_ERR_UNSUPPORTED;
+  if (num_seqs == 0 || total_q == 0 || max_seqlen_q == 0) return ATTN_OK;  // nothing to compute
+  if (!out || !q || !k_cache || !v_cache || !block_table || !query_start_loc || !seq_lens)
+    return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache))
+    return ATTN_ERR_INVALID_ARG;
+  const int64_t pages_needed = ((int64_t)max_seqlen_k + block_size - 1) / block_size;
+  if (block_table_stride < 1 || block_table_stride < pages_needed) return ATTN_ERR_INVALID_ARG;
+  const int group = num_q_heads / num_kv_heads;
+  const bool pair_heads = group % 2 == 0;
+  const int64_t row_blocks = ((int64_t)max_seqlen_q + 127) / 128;
+  const int64_t gz = pair_heads ? row_blocks : (row_blocks + 1) / 2;
+  const int64_t gx = pair_heads ? num_q_heads / 2 : num_q_heads;
+  if (num_seqs > 65535 || gz > 65535 || gx > 2147483647) return ATTN_ERR_UNSUPPORTED;
+
+  attn_status_t st = check_device();
+  if (st != ATTN_OK) return st;
+
+  attn::PrefillParams p;
+  std::memset(&p, 0, sizeof(p));
+  const bool bf16 = dtype == ATTN_BF16;
+  const cuuint64_t d = (cuuint64_t)head_size;
+  {
+    const cuuint64_t dims[3] = {d, (cuuint64_t)num_q_heads, (cuuint64_t)total_q};
+    const cuuint64_t strides[2] = {d * 2, d * 2 * (cuuint64_t)num_q_heads};
+    const cuuint32_t box[3] = {64, 1, 128};
+    if (!encode(&p.tm_q, bf16, 3, dims, strides, box, q, CU_TENSOR_MAP_SWIZZLE_128B)) return ATTN_ERR_CUDA;
+  }
+  {
+    const cuuint64_t dims[4] = {d, (cuuint64_t)num_kv_heads, (cuuint64_t)block_size,
+                                (cuuint64_t)num_blocks};
+    const cuuint64_t strides[3] = {d * 2, d * 2 * (cuuint64_t)num_kv_heads,
+                                   d * 2 * (cuuint64_t)num_kv_heads * (cuuint64_t)block_size};
+    const cuuint32_t box[4] = {64, 1, (cuuint32_t)(block_size < 128 ? block_size : 128), 1};
+    if (!encode(&p.tm_k, bf16, 4, dims, strides, box, k_cache, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode(&p.tm_v, bf16, 4, dims, strides, box, v_cache, CU_TENSOR_MAP_SWIZZLE_128B))
+      return ATTN_ERR_CUDA;
+  }
+  p.out = out;
+  p.lse = lse_out;
+  p.status = status_dev;
+  p.block_table = block_table;
+  p.query_start_loc = query_start_loc;
+  p.seq_lens = seq_lens;
+  p.bt_stride = block_table_stride;
+  p.num_seqs = num_seqs;
+  p.max_seqlen_q = max_seqlen_q;
+  p.max_seqlen_k = max_seqlen_k;
+  p.total_q = total_q;
+  p.num_q_heads = num_q_heads;
+  p.num_kv_heads = num_kv_heads;
+  p.block_size = block_size;
+  p.num_blocks = num_blocks;
+  p.box_rows = block_size < 128 ? block_size : 128;
+  p.pair_heads = pair_heads ? 1 : 0;
+  p.causal = causal;
+  p.rounding = (int32_t)rounding;
+  p.scale_log2 = scale * kLog2e;
+
+  dim3 grid((unsigned)gx, (unsigned)num_seqs, (unsigned)gz);
+  cudaError_t e = attn::launch_prefill(p, head_size, bf16, grid, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+size_t attn_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t head_size,
+                                  int32_t num_splits) {
+  if (num_seqs <= 0 || num_q_heads <= 0 || head_size <= 0 || num_splits <= 1) return 0;
+  const size_t rows = (size_t)num_seqs * (size_t)num_q_heads * (size_t)num_splits;
+  return rows * (size_t)head_size * sizeof(float) + rows * 2 * sizeof(float);
+}
+
+attn_status_t attn_fwd_decode(void* out, const void* q, const void* k_cache, const void* v_cache,
+                              const int32_t* block_table, int32_t block_table_stride,
+                              const int32_t* seq_lens, int32_t num_seqs, int32_t max_seqlen_k,
+                              int32_t num_q_heads, int32_t num_kv_heads, int32_t head_size,
+                              int32_t block_size, int32_t num_blocks, float scale,
+                              int32_t num_splits, attn_dtype_t dtype, attn_round_t rounding,
+                              float* lse_out, void* workspace, size_t workspace_bytes,
+                              int32_t* status_dev, void* stream) {
+  if (num_seqs < 0 || max_seqlen_k < 0) return ATTN_ERR_INVALID_ARG;
+  if (num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0) return ATTN_ERR_INVALID_ARG;
+  if (dtype != ATTN_F16 && dtype != ATTN_BF16) return ATTN_ERR_INVALID_ARG;
+  if (rounding < ATTN_RTNE || rounding > ATTN_OUT_F32) return ATTN_ERR_INVALID_ARG;
+  if (!valid_scale(scale)) return ATTN_ERR_INVALID_ARG;
+  if (block_size <= 0 || num_blocks <= 0) return ATTN_ERR_INVALID_ARG;
+  if (num_splits < 1 || num_splits > 64) return ATTN_ERR_INVALID_ARG;
+  if (head_size != 64 && head_size != 128) return ATTN_ERR_UNSUPPORTED;
+  if (block_size % 16 != 0) return ATTN_ERR_UNSUPPORTED;
+  if (num_seqs == 0) return ATTN_OK;
+  if (!out || !q || !k_cache || !v_cache || !block_table || !seq_lens) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache))
+    return ATTN_ERR_INVALID_ARG;
+  const int64_t pages_needed = ((int64_t)max_seqlen_k + block_size - 1) / block_size;
+  if (block_table_stride < 1 || block_table_stride < pages_needed) return ATTN_ERR_INVALID_ARG;
+  const size_t need = attn_decode_workspace_size(num_seqs, num_q_heads, head_size, num_splits);
+  if (need > 0 && (!workspace || workspace_bytes < need || !aligned16(workspace)))
+    return ATTN_ERR_WORKSPACE;
+  if (num_seqs > 65535 || (int64_t)num_q_heads > 65535) return ATTN_ERR_UNSUPPORTED;
+
+  attn_status_t st = check_device();
+  if (st != ATTN_OK) return st;
+
+  attn::DecodeParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.q = q;
+  p.k_cache = k_cache;
+  p.v_cache = v_cache;
+  p.out = out;
+  p.lse = lse_out;
+  p.status = status_dev;
+  p.block_table = block_table;
+  p.seq_lens = seq_lens;
+  if (need > 0) {
+    const size_t rows = (size_t)num_seqs * num_q_heads * num_splits;
+    p.part_o = static_cast<float*>(workspace);
+    p.part_ml = p.part_o + rows * (size_t)head_size;
+  }
+  p.bt_stride = block_table_stride;
+  p.num_seqs = num_seqs;
+  p.max_seqlen_k = max_seqlen_k;
+  p.num_q_heads = num_q_heads;
+  p.num_kv_heads = num_kv_heads;
+  p.block_size = block_size;
+  p.num_blocks = num_blocks;
+  p.num_splits = num_splits;
+  p.rounding = (int32_t)rounding;
+  p.scale_log2 = scale * kLog2e;
+  cudaError_t e = attn::launch_decode(p, head_size, dtype == ATTN_BF16, num_q_heads / num_kv_heads,
+                                      static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+attn_status_t attn_round_f32(void* out, const float* in, int64_t n, attn_dtype_t dtype,
+                             attn_round_t rounding, void* stream) {
+  if (n < 0) return ATTN_ERR_INVALID_ARG;
+  if (dtype != ATTN_F16 && dtype != ATTN_BF16) return ATTN_ERR_INVALID_ARG;
+  if (rounding < ATTN_RTNE || rounding > ATTN_RTZ) return ATTN_ERR_INVALID_ARG;
+  if (n == 0) return ATTN_OK;
+  if (!out || !in) return ATTN_ERR_INVALID_ARG;
+  attn_status_t st = check_device();
+  if (st != ATTN_OK) return st;
+  cudaError_t e = attn::launch_round(out, in, n, dtype == ATTN_BF16, (int)rounding,
+                                     static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,78 @@
+// attn_internal.h -- parameter blocks shared by the C-ABI layer and the
+// kernel launchers (not part of the public interface).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstddef>
+#include <cstdint>
+
+namespace attn {
+
+// One prefill launch.  Tensor maps are encoded on the host (attn_api.cu).
+struct PrefillParams {
+  CUtensorMap tm_q;   // Q  [total_q, Hq, d]: dims (d, Hq, total_q), box (64, 1, 128), 128B swizzle
+  CUtensorMap tm_k;   // K  [num_blocks, bs, Hkv, d]: dims (d, Hkv, bs, num_blocks), box (64, 1, R, 1)
+  CUtensorMap tm_v;   // V  same as K
+  void* out;          // [total_q, Hq, d] 16-bit, or fp32 when rounding == 3
+  float* lse;         // [total_q, Hq] or nullptr
+  int32_t* status;    // device status word or nullptr
+  const int32_t* block_table;
+  const int32_t* query_start_loc;
+  const int32_t* seq_lens;
+  int32_t bt_stride;
+  int32_t num_seqs;
+  int32_t max_seqlen_q;
+  int32_t max_seqlen_k;
+  int32_t total_q;
+  int32_t num_q_heads;
+  int32_t num_kv_heads;
+  int32_t block_size;
+  int32_t num_blocks;
+  int32_t box_rows;     // rows of one K/V TMA box = min(block_size, 128)
+  int32_t pair_heads;   // 1: the two Q tiles of a CTA are two heads of one group
+  int32_t causal;
+  int32_t rounding;     // 0 RTNE, 1 RTNA, 2 RTZ, 3 fp32 output
+  float scale_log2;     // tau * log2(e)
+};
+
+struct DecodeParams {
+  const void* q;        // [num_seqs, Hq, d]
+  const void* k_cache;  // [num_blocks, bs, Hkv, d]
+  const void* v_cache;  // [num_blocks, bs, Hkv, d]
+  void* out;            // [num_seqs, Hq, d] 16-bit, or fp32 when rounding == 3
+  float* lse;           // [num_seqs, Hq] or nullptr
+  int32_t* status;
+  const int32_t* block_table;
+  const int32_t* seq_lens;
+  float* part_o;        // [num_seqs, Hq, splits, d] un-normalised partial outputs
+  float* part_ml;       // [num_seqs, Hq, splits, 2] (running max in log2 units, denominator)
+  int32_t bt_stride;
+  int32_t num_seqs;
+  int32_t max_seqlen_k;
+  int32_t num_q_heads;
+  int32_t num_kv_heads;
+  int32_t block_size;
+  int32_t num_blocks;
+  int32_t num_splits;
+  int32_t rounding;
+  float scale_log2;
+};
+
+// Launchers return a cudaError_t from the launch.
+cudaError_t launch_prefill(const PrefillParams& p, int head_size, bool bf16, dim3 grid,
+                           cudaStream_t stream);
+cudaError_t launch_decode(const DecodeParams& p, int head_size, bool bf16, int group,
+                          cudaStream_t stream);
+cudaError_t launch_round(void* out, const float* in, int64_t n, bool bf16, int mode,
+                         cudaStream_t stream);
+
+// In-kernel error codes written to the status word (same values as the
+// public attn_status_t).
+enum : int32_t { kStatusBadArg = 1, kStatusBadBlockTable = 5, kStatusTimeout = 6 };
+
+__device__ __forceinline__ void report_status(int32_t* status, int32_t code) {
+  if (status) atomicCAS(status, 0, code);
+}
+
+}  // namespace attn

@@ -1,0 +1,457 @@
+// prefill_tcgen05.cu -- fused SDPA forward for prefill / dense attention on
+// sm_103a: O = softmax(tau * Q K^T + mask) V by the online-softmax recurrence
+// ("gfx942 unified attention, from the math up", sec. 3), over a paged K/V
+// cache read through a block table (sec. 5), with the bottom-right causal mask
+// and the early exit over fully-future key tiles (sec. 4), MHA and GQA.
+//
+// One CTA owns two 128-row query tiles that share one KV head: two heads of a
+// GQA group over the same rows (balanced ping-pong), or, when the group size
+// is odd, two consecutive row blocks of one head.  Warp roles:
+//   warp 0      TMA producer: Q tiles once, then K_j / V_j tiles (128 keys)
+//               into a ring of shared-memory slots (128-byte swizzle);
+//   warp 1      owns TMEM (512 columns) and issues the tcgen05 MMAs:
+//               S_t = Q_t K_j^T (fp32 in TMEM), O_t += P_t V_j (P from TMEM);
+//   warps 4-7   softmax for tile 0, warps 8-11 for tile 1 (one thread per
+//               query row, tcgen05.ld of its row of S): mask, running max,
+//               exp2, running denominator, P (16-bit) written back over S,
+//               rescale of O in TMEM when the max moved, and the epilogue
+//               O / l -> RTNE / RTNA / RTZ rounding -> global store.
+// The MMA issue order S_0(j), S_1(j), PV_0(j), S_0(j+1), PV_1(j), S_1(j+1) ...
+// lets one tile's softmax overlap the other tile's matrix products.
+//
+// TMEM map (columns): S_0 [0,128), S_1 [128,256), O_0 [256,256+d),
+// O_1 [256+d, 256+2d).  P_t overwrites the first 64 columns of S_t as packed
+// 16-bit pairs and is the A operand of the P.V product.
+
+#include "attn_internal.h"
+#include "round16.cuh"
+#include "sm103_ptx.cuh"
+
+namespace attn {
+namespace {
+
+constexpr int kBM = 128;        // query rows per tile
+constexpr int kBN = 128;        // keys per KV tile
+constexpr int kThreads = 384;   // 12 warps
+constexpr float kLn2 = 0.693147180559945309f;
+
+template <int D>
+struct PrefillLayout {
+  static constexpr int kHalves = D / 64;             // 128-byte swizzle spans 64 elements
+  static constexpr int kHalfBytes = 128 * 128;       // 128 rows x 128 bytes
+  static constexpr int kTileBytes = kHalves * kHalfBytes;
+  static constexpr int kStages = D == 128 ? 4 : 8;   // K/V ring slots
+  static constexpr int kQOff = 0;
+  static constexpr int kRingOff = 2 * kTileBytes;
+  static constexpr int kBarOff = kRingOff + kStages * kTileBytes;
+  static constexpr int kNumBars = 2 + 2 * kStages + 2 + 2 + 2 + 1;
+  static constexpr int kMiscOff = kBarOff + kNumBars * 8;
+  static constexpr int kSmemBytes = kMiscOff + 16 + 1024;  // + slack for 1024-byte alignment
+  static __device__ __forceinline__ constexpr uint32_t s_col(int t) { return t ? 128u : 0u; }
+  static __device__ __forceinline__ constexpr uint32_t o_col(int t) { return t ? 256u + D : 256u; }
+  static constexpr uint32_t kTmemCols = 512;
+};
+
+// Waits without regard to the abort flag: used on the way out to make sure no
+// asynchronous copy or MMA still targets this CTA's memory.
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_test(bar, parity)) {
+    if (global_timer_ns() - t0 > kWaitLimitNs) break;
+  }
+}
+
+template <int D, bool BF16>
+__global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_constant__ PrefillParams p) {
+  using L = PrefillLayout<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* smem = smem_raw + (base - raw);
+  const uint32_t sQ = base + L::kQOff;
+  const uint32_t sRing = base + L::kRingOff;
+  const uint32_t bars = base + L::kBarOff;
+  const uint32_t bar_q_full = bars;                                  // [2]
+  const uint32_t bar_kv_full = bars + 8u * 2u;                       // [kStages]
+  const uint32_t bar_kv_empty = bars + 8u * (2u + L::kStages);       // [kStages]
+  const uint32_t bar_s_full = bars + 8u * (2u + 2u * L::kStages);    // [2]
+  const uint32_t bar_p_full = bar_s_full + 16u;                      // [2]
+  const uint32_t bar_o_full = bar_s_full + 32u;                      // [2]
+  const uint32_t bar_mma_done = bar_s_full + 48u;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMiscOff + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  // ------------------------------------------------------------ work item
+  const int b = blockIdx.y;
+  const int q_begin = p.query_start_loc[b];
+  const int q_end = p.query_start_loc[b + 1];
+  const int Sq = q_end - q_begin;
+  const int Sk = p.seq_lens[b];
+  if (q_begin < 0 || Sq < 0 || Sq > p.max_seqlen_q || q_end > p.total_q || Sk < 0 ||
+      Sk > p.max_seqlen_k) {
+    if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.z == 0) report_status(p.status, kStatusBadArg);
+    return;
+  }
+  const int n_rb = (Sq + kBM - 1) / kBM;
+  int head[2], row0[2], rows[2], n_kv[2], lim_lo[2];
+  if (p.pair_heads) {
+    if ((int)blockIdx.z >= n_rb) return;
+    const int rb = n_rb - 1 - (int)blockIdx.z;   // heaviest (last) row block first
+    for (int t = 0; t < 2; ++t) {
+      head[t] = 2 * (int)blockIdx.x + t;
+      row0[t] = rb * kBM;
+    }
+  } else {
+    const int units = (n_rb + 1) / 2;
+    if ((int)blockIdx.z >= units) return;
+    const int u = units - 1 - (int)blockIdx.z;
+    for (int t = 0; t < 2; ++t) {
+      head[t] = (int)blockIdx.x;
+      row0[t] = (2 * u + t) * kBM;
+    }
+  }
+  const int off = Sk - Sq;  // bottom-right alignment: row i sees keys j <= i + off
+#pragma unroll
+  for (int t = 0; t < 2; ++t) {
+    rows[t] = row0[t] < Sq ? min(kBM, Sq - row0[t]) : 0;
+    n_kv[t] = 0;
+    lim_lo[t] = 0;
+    if (rows[t] > 0) {
+      const int last = row0[t] + rows[t] - 1;
+      const int lim = p.causal ? min(Sk, last + off + 1) : Sk;
+      n_kv[t] = lim > 0 ? (lim + kBN - 1) / kBN : 0;
+      lim_lo[t] = p.causal ? min(Sk, row0[t] + off + 1) : Sk;
+    }
+  }
+  const int n_kv_max = max(n_kv[0], n_kv[1]);
+  const int group = p.num_q_heads / p.num_kv_heads;
+  const int kvh = head[0] / group;
+
+  // ------------------------------------------------------------ setup
+  if (threadIdx.x == 0) {
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(bar_q_full + 8u * t, 1);
+      mbar_init(bar_s_full + 8u * t, 1);
+      mbar_init(bar_p_full + 8u * t, kBM);
+      mbar_init(bar_o_full + 8u * t, 1);
+    }
+    for (int s = 0; s < L::kStages; ++s) {
+      mbar_init(bar_kv_full + 8u * s, 1);
+      mbar_init(bar_kv_empty + 8u * s, 1);
+    }
+    mbar_init(bar_mma_done, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&p.tm_q);
+    tma_prefetch_desc(&p.tm_k);
+    tma_prefetch_desc(&p.tm_v);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), L::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------- producer
+    if (lane == 0) {
+      for (int t = 0; t < 2; ++t) {
+        if (n_kv[t] == 0) continue;
+        const uint32_t bar = bar_q_full + 8u * t;
+        mbar_arrive_expect_tx(bar, L::kTileBytes);
+        for (int h = 0; h < L::kHalves; ++h)
+          tma_load_3d(sQ + t * L::kTileBytes + h * L::kHalfBytes, &p.tm_q, bar, h * 64, head[t],
+                      q_begin + row0[t]);
+      }
+      const int bs = p.block_size;
+      const int n_pages = (Sk + bs - 1) / bs;
+      const int32_t* bt = p.block_table + (int64_t)b * p.bt_stride;
+      int filled[L::kStages];
+#pragma unroll
+      for (int s = 0; s < L::kStages; ++s) filled[s] = 0;
+      for (int i = 0; i < 2 * n_kv_max; ++i) {
+        const int j = i >> 1;
+        const int s = i % L::kStages;
+        const int u = i / L::kStages;
+        if (u > 0 && !mbar_wait(bar_kv_empty + 8u * s, (u - 1) & 1, abort_flag)) break;
+        const uint32_t dst = sRing + s * L::kTileBytes;
+        const uint32_t bar = bar_kv_full + 8u * s;
+        const CUtensorMap* tm = (i & 1) ? &p.tm_v : &p.tm_k;
+        const int key0 = j * kBN;
+        if (bs >= kBN) {
+          int page = bt[key0 / bs];
+          if (page < 0 || page >= p.num_blocks) report_status(p.status, kStatusBadBlockTable);
+          mbar_arrive_expect_tx(bar, L::kTileBytes);
+          for (int h = 0; h < L::kHalves; ++h)
+            tma_load_4d(dst + h * L::kHalfBytes, tm, bar, h * 64, kvh, key0 % bs, page);
+        } else {
+          const int first = key0 / bs;
+          const int cnt = min(kBN / bs, n_pages - first);
+          mbar_arrive_expect_tx(bar, (uint32_t)(cnt * L::kHalves * bs * 128));
+          for (int r = 0; r < cnt; ++r) {
+            const int page = bt[first + r];
+            if (page < 0 || page >= p.num_blocks) report_status(p.status, kStatusBadBlockTable);
+            for (int h = 0; h < L::kHalves; ++h)
+              tma_load_4d(dst + h * L::kHalfBytes + r * bs * 128, tm, bar, h * 64, kvh, 0, page);
+          }
+        }
+        filled[s] = u + 1;
+      }
+      // make sure no copy into this CTA's shared memory is still in flight
+      for (int s = 0; s < L::kStages; ++s)
+        if (filled[s] > 0) drain_wait(bar_kv_full + 8u * s, (filled[s] - 1) & 1);
+      for (int t = 0; t < 2; ++t)
+        if (n_kv[t] > 0) drain_wait(bar_q_full + 8u * t, 0);
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------- MMA issuer
+    const bool leader = lane == 0;
+    const uint32_t idesc_s = make_idesc_f16(BF16, kBM, kBN, false);
+    const uint32_t idesc_pv = make_idesc_f16(BF16, kBM, D, true);
+    auto issue_s = [&](int t, int slot) {
+      const uint32_t a0 = sQ + t * L::kTileBytes;
+      const uint32_t b0 = sRing + slot * L::kTileBytes;
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t o = (kk >> 2) * L::kHalfBytes + (kk & 3) * 32;
+        umma_ss(tmem + L::s_col(t), make_sdesc_sw128(a0 + o, 16, 1024),
+                make_sdesc_sw128(b0 + o, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
+      }
+    };
+    auto issue_pv = [&](int t, int slot, bool acc) {
+      const uint32_t b0 = sRing + slot * L::kTileBytes;
+#pragma unroll
+      for (int kk = 0; kk < kBN / 16; ++kk) {
+        umma_ts(tmem + L::o_col(t), tmem + L::s_col(t) + kk * 8,
+                make_sdesc_sw128(b0 + kk * 16 * 128, L::kHalfBytes, 1024), idesc_pv,
+                (acc || kk > 0) ? 1u : 0u);
+      }
+    };
+    bool ok = true;
+    for (int t = 0; t < 2 && ok; ++t)
+      if (n_kv[t] > 0) ok = mbar_wait(bar_q_full + 8u * t, 0, abort_flag);
+    if (ok && n_kv_max > 0) {
+      ok = mbar_wait(bar_kv_full, 0, abort_flag);  // K_0: item 0, slot 0, first fill
+      if (ok) {
+        tc_fence_after();
+        for (int t = 0; t < 2; ++t) {
+          if (n_kv[t] == 0) continue;
+          if (leader) {
+            issue_s(t, 0);
+            umma_commit(bar_s_full + 8u * t);
+          }
+        }
+        if (leader) umma_commit(bar_kv_empty);
+        __syncwarp();
+      }
+    }
+    for (int j = 0; ok && j < n_kv_max; ++j) {
+      const int iv = 2 * j + 1;
+      const int sv = iv % L::kStages;
+      if (!mbar_wait(bar_kv_full + 8u * sv, (iv / L::kStages) & 1, abort_flag)) { ok = false; break; }
+      tc_fence_after();
+      if ((j + 1) * kBN > Sk) {
+        // keys at or past kv_len in the last tile: their V rows may hold
+        // anything (NaN included); P is 0 there but 0 * NaN is not, so zero them.
+        const int r0 = Sk - j * kBN;
+        uint8_t* vt = smem + (sRing - base) + sv * L::kTileBytes;
+        for (int idx = lane; idx < (kBN - r0) * L::kHalves * 8; idx += 32) {
+          const int chunk = idx & 7;
+          const int rh = idx >> 3;
+          const int h = rh % L::kHalves;
+          const int r = r0 + rh / L::kHalves;
+          *reinterpret_cast<uint4*>(vt + h * L::kHalfBytes + r * 128 + chunk * 16) =
+              make_uint4(0u, 0u, 0u, 0u);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+      }
+      bool k_next = false;
+      int sk_next = 0;
+      for (int t = 0; t < 2 && ok; ++t) {
+        if (j >= n_kv[t]) continue;
+        if (!mbar_wait(bar_p_full + 8u * t, j & 1, abort_flag)) { ok = false; break; }
+        tc_fence_after();
+        if (leader) issue_pv(t, sv, j > 0);
+        if (j + 1 < n_kv[t]) {
+          if (!k_next) {
+            const int ik = 2 * (j + 1);
+            sk_next = ik % L::kStages;
+            if (!mbar_wait(bar_kv_full + 8u * sk_next, (ik / L::kStages) & 1, abort_flag)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            k_next = true;
+          }
+          if (leader) {
+            issue_s(t, sk_next);
+            umma_commit(bar_s_full + 8u * t);
+          }
+        } else if (leader) {
+          umma_commit(bar_o_full + 8u * t);
+        }
+        __syncwarp();
+      }
+      if (leader) {
+        umma_commit(bar_kv_empty + 8u * sv);
+        if (k_next) umma_commit(bar_kv_empty + 8u * sk_next);
+      }
+      __syncwarp();
+    }
+    // no MMA may still be running when TMEM is released
+    if (leader) umma_commit(bar_mma_done);
+    __syncwarp();
+    drain_wait(bar_mma_done, 0);
+  } else if (warp >= 4) {
+    // ---------------------------------------------------------- softmax + epilogue
+    const int t = (warp - 4) >> 2;
+    const int wq = warp & 3;
+    const int r = wq * 32 + lane;
+    const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+    const uint32_t tS = tmem + lane_off + L::s_col(t);
+    const uint32_t tO = tmem + lane_off + L::o_col(t);
+    const int i_row = row0[t] + r;
+    const int key_lim = p.causal ? min(Sk, i_row + off + 1) : Sk;
+    const float sl2 = p.scale_log2;
+    float m = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < n_kv[t]; ++j) {
+      if (!mbar_wait(bar_s_full + 8u * t, j & 1, abort_flag)) { ok = false; break; }
+      tc_fence_after();
+      uint32_t s[4][32];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld32(tS + 32 * c, s[c]);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld_wait(s[c]);
+      if ((j + 1) * kBN > lim_lo[t]) {
+        const int cl = key_lim - j * kBN;  // columns >= cl are masked for this row
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            if (32 * c + e >= cl) s[c][e] = 0xFF800000u;  // -inf
+      }
+      float mx = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+#pragma unroll
+        for (int e = 0; e < 32; ++e) mx = fmaxf(mx, __uint_as_float(s[c][e]));
+      const float m_new = fmaxf(m, mx * sl2);
+      const float m_use = m_new == -INFINITY ? 0.f : m_new;
+      const float alpha = fast_exp2(m - m_use);
+      float rs = 0.f;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const float p0 = fast_exp2(fmaf(__uint_as_float(s[c][2 * e]), sl2, -m_use));
+          const float p1 = fast_exp2(fmaf(__uint_as_float(s[c][2 * e + 1]), sl2, -m_use));
+          rs += p0 + p1;
+          pk[e] = BF16 ? pack_bf16x2_rn(p0, p1) : pack_f16x2_rn(p0, p1);
+        }
+        tmem_st16(tS + 16 * c, pk);
+      }
+      l = l * alpha + rs;
+      if (j > 0 && __any_sync(0xFFFFFFFFu, alpha != 1.f)) {
+        // O_t is final for tile j-1 here: S_t(j) was issued after PV_t(j-1)
+        // and its commit covers every earlier MMA.
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32(tO + 32 * c, o);
+          tmem_ld_wait(o);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+          tmem_st32(tO + 32 * c, o);
+        }
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(bar_p_full + 8u * t);
+      m = m_new;
+    }
+    if (ok && n_kv[t] > 0) {
+      ok = mbar_wait(bar_o_full + 8u * t, 0, abort_flag);
+      tc_fence_after();
+    }
+    if (ok) {
+      const bool row_ok = r < rows[t];
+      const int64_t tok = (int64_t)q_begin + row0[t] + r;
+      const int64_t obase = (tok * p.num_q_heads + head[t]) * D;
+      const float inv_l = l > 0.f ? 1.f / l : 0.f;
+#pragma unroll 1
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t o[32];
+        if (n_kv[t] > 0) {
+          tmem_ld32(tO + 32 * c, o);
+          tmem_ld_wait(o);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] = 0u;
+        }
+        if (!row_ok) continue;
+        if (p.rounding == 3) {
+          float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + obase + 32 * c);
+#pragma unroll
+          for (int v = 0; v < 8; ++v)
+            dst[v] = make_float4(__uint_as_float(o[4 * v]) * inv_l, __uint_as_float(o[4 * v + 1]) * inv_l,
+                                 __uint_as_float(o[4 * v + 2]) * inv_l, __uint_as_float(o[4 * v + 3]) * inv_l);
+        } else {
+          uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + obase + 32 * c);
+          uint32_t w[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            w[e] = round_out_x2<BF16>(__uint_as_float(o[2 * e]) * inv_l,
+                                      __uint_as_float(o[2 * e + 1]) * inv_l, p.rounding);
+#pragma unroll
+          for (int v = 0; v < 4; ++v) dst[v] = make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
+        }
+      }
+      if (row_ok && p.lse)
+        p.lse[tok * p.num_q_heads + head[t]] = l > 0.f ? m * kLn2 + logf(l) : -INFINITY;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, L::kTmemCols);
+  }
+  if (threadIdx.x == 0 && *abort_flag) report_status(p.status, kStatusTimeout);
+}
+
+template <int D, bool BF16>
+cudaError_t launch_one(const PrefillParams& p, dim3 grid, cudaStream_t stream) {
+  using L = PrefillLayout<D>;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(prefill_kernel<D, BF16>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  prefill_kernel<D, BF16><<<grid, kThreads, L::kSmemBytes, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_prefill(const PrefillParams& p, int head_size, bool bf16, dim3 grid,
+                           cudaStream_t stream) {
+  if (head_size == 128) return bf16 ? launch_one<128, true>(p, grid, stream) : launch_one<128, false>(p, grid, stream);
+  if (head_size == 64) return bf16 ? launch_one<64, true>(p, grid, stream) : launch_one<64, false>(p, grid, stream);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace attn

@@ -1,0 +1,503 @@
+"""Benchmark of the fused SDPA forward on one or more GB300s.
+
+One step is one pass of the whole hot path over one batch of synthetic input:
+  1. a causal GQA prefill through a paged cache -- workload
+     prefill_causal_bf16_gqa_s2048: bf16, B=1, Hq=32, Hkv=8 (GQA 4:1),
+     Sq=Sk=2048, d=128, block size 64 with a randomly permuted block table;
+  2. one split-KV decode step -- workload decode_bf16_b64_paged16: bf16,
+     B=64, Hq=32, Hkv=8, d=128, kv lengths uniform in [512, 8192], block
+     size 16, shared permuted pool, 8 splits + log-sum-exp combine.
+Inputs are seeded synthetic N(0,1) tensors already resident in HBM when the
+timed region starts.  L2 is flushed before every step (a 256 MiB write).
+
+Reported (one JSON line on rank 0):
+  value        prefill attention TFLOP/s (unmasked FLOPs, 4*d per visible
+               (query, key) pair per query head) from CUDA events around the
+               prefill launches, summed over all ranks;
+  decode       decode KV GB/s (K+V bytes read + Q + O) from CUDA events around
+               the decode call (split kernel + combine kernel);
+  roofline     for the kernel with the larger share of device time: achieved
+               vs the measured peak (HBM copy GB/s, or dense bf16 TFLOP/s);
+  e2e          the same metric with host buffers: per step the host->device
+               copy of the step's inputs from pinned memory, the calls, and
+               the device->host copy of the outputs, all timed;
+  cpu_baseline the fp64 CPU oracle on a bounded row sample of the same
+               workloads (rank 0, single-GPU runs only).
+`--impl reference` times the oracle instead (the reference arm).
+Multi-GPU: every rank runs its own copy of the workload (independent
+problems, no collective on the data path); value is the sum over ranks of the
+work divided by the slowest rank's time (weak scaling).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import attn_inputs  # noqa: E402
+
+METRIC = "prefill attn TFLOP/s & decode KV GB/s on 1 GB300; % of tensor/HBM roofline"
+PREFILL_WL = "prefill_causal_bf16_gqa_s2048"
+DECODE_WL = "decode_bf16_b64_paged16"
+DECODE_SPLITS = 8
+L2_FLUSH_BYTES = 256 << 20
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ----------------------------------------------------------------------------
+# algorithmic work
+# ----------------------------------------------------------------------------
+
+def visible_pairs(q_lens, kv_lens, causal: bool) -> int:
+    """(query row, key) pairs left visible by the mask, per query head;
+    bottom-right causal alignment: row i of a sequence sees j <= i + Sk - Sq."""
+    tot = 0
+    for sq, sk in zip(q_lens, kv_lens):
+        if not causal:
+            tot += sq * sk
+            continue
+        off = sk - sq
+        i = np.arange(sq, dtype=np.int64)
+        tot += int(np.clip(np.minimum(sk, i + off + 1), 0, None).sum())
+    return tot
+
+
+def prefill_flops(prob) -> float:
+    return 4.0 * prob.head_size * prob.num_q_heads * visible_pairs(prob.q_lens, prob.kv_lens,
+                                                                   prob.causal)
+
+
+def decode_bytes(prob) -> float:
+    el = 2
+    kv = 2.0 * sum(prob.kv_lens) * prob.num_kv_heads * prob.head_size * el
+    qo = 2.0 * prob.num_seqs * prob.num_q_heads * prob.head_size * el
+    return kv + qo
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ----------------------------------------------------------------------------
+# clocks
+# ----------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.samples = []
+        self.proc = None
+        self.gpu = gpu_index
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), line.strip()))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=2)
+
+    def summary(self, t0: float, t1: float):
+        def parse(line):
+            parts = [x.strip() for x in line.split(",")]
+            try:
+                return (float(parts[0]), float(parts[1]), parts[3:])
+            except Exception:
+                return None
+        inside = [parse(l) for t, l in self.samples if t0 <= t <= t1]
+        inside = [x for x in inside if x]
+        window = "timed"
+        if not inside:
+            inside = [x for x in (parse(l) for _, l in self.samples) if x]
+            window = "whole run"
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for _, _, flags in inside:
+            for n, v in zip(names, flags[1:5]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(x[0] for x in inside),
+                "sm_max_mhz": max(x[1] for x in inside), "reasons": sorted(reasons),
+                "samples": len(inside), "window": window}
+
+
+# ----------------------------------------------------------------------------
+# the library arm
+# ----------------------------------------------------------------------------
+
+def make_problems(seed: int):
+    return attn_inputs.workload(PREFILL_WL, seed=seed), attn_inputs.workload(DECODE_WL, seed=seed)
+
+
+def device_args(prob, dev):
+    return {k: getattr(prob, k).to(dev) for k in ("q", "k_cache", "v_cache", "block_table",
+                                                  "query_start_loc", "seq_lens")}
+
+
+def run_ours(args, rank, world, dev):
+    import attention_forward_sdpa_gb300 as attn
+
+    attn.load_library()
+    pp, dp = make_problems(seed=rank)
+    pt, dt = device_args(pp, dev), device_args(dp, dev)
+    p_out = torch.empty_like(pt["q"])
+    d_out = torch.empty_like(dt["q"])
+    ws_n = attn.attn_decode_workspace_size(dp.num_seqs, dp.num_q_heads, dp.head_size, DECODE_SPLITS)
+    ws = torch.empty(ws_n, dtype=torch.uint8, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def do_prefill(t, out):
+        attn.attn_fwd_prefill(out, t["q"], t["k_cache"], t["v_cache"], t["block_table"],
+                              t["query_start_loc"], t["seq_lens"], max_seqlen_q=pp.max_seqlen_q,
+                              max_seqlen_k=pp.max_seqlen_k, scale=pp.scale, causal=True,
+                              stream=stream)
+
+    def do_decode(t, out):
+        attn.attn_fwd_decode(out, t["q"], t["k_cache"], t["v_cache"], t["block_table"],
+                             t["seq_lens"], max_seqlen_k=dp.max_seqlen_k, scale=dp.scale,
+                             num_splits=DECODE_SPLITS, workspace=ws, stream=stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        do_prefill(pt, p_out)
+        do_decode(dt, d_out)
+    torch.cuda.synchronize(dev)
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    ev_all = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    sampler = ClockSampler(dev.index if dev.index is not None else 0)
+    sampler.start()
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    t_wall0 = time.time()
+    ev_all[0].record(stream)
+    for k in range(K):
+        flush.zero_()
+        ev[k][0].record(stream)
+        do_prefill(pt, p_out)
+        ev[k][1].record(stream)
+        do_decode(dt, d_out)
+        ev[k][2].record(stream)
+    ev_all[1].record(stream)
+    torch.cuda.synchronize(dev)
+    t_wall1 = time.time()
+    barrier(world)
+    sampler.stop()
+
+    p_ms = [ev[k][0].elapsed_time(ev[k][1]) for k in range(K)]
+    d_ms = [ev[k][1].elapsed_time(ev[k][2]) for k in range(K)]
+    step_ms = ev_all[0].elapsed_time(ev_all[1]) / K
+    p_ms_tot, d_ms_tot = sum(p_ms), sum(d_ms)
+    # slowest rank decides
+    p_ms_tot, d_ms_tot, step_ms = max_over_ranks(world, dev, [p_ms_tot, d_ms_tot, step_ms])
+
+    flops = prefill_flops(pp)
+    dbytes = decode_bytes(dp)
+    tflops = world * flops * K / (p_ms_tot * 1e-3) / 1e12
+    gbs = world * dbytes * K / (d_ms_tot * 1e-3) / 1e9
+    peaks, peak_src = load_peaks()
+    p_avg_s = p_ms_tot / K * 1e-3
+    d_avg_s = d_ms_tot / K * 1e-3
+    roof_p = {"kernel": "prefill_kernel<128,bf16>", "bound": "tensor",
+              "achieved": flops / p_avg_s / 1e12, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+              "frac": flops / p_avg_s / 1e12 / peaks["bf16_tflops"], "traffic": None,
+              "peak_source": f"{peak_src} bf16 burst", "avg_launch_us": p_avg_s * 1e6,
+              "algorithmic_per_launch": flops}
+    roof_d = {"kernel": "decode_split_kernel<128,bf16,4> + decode_combine_kernel", "bound": "hbm",
+              "achieved": dbytes / d_avg_s / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+              "frac": dbytes / d_avg_s / 1e9 / peaks["hbm_gbs"], "traffic": None,
+              "peak_source": f"{peak_src} HBM copy", "avg_launch_us": d_avg_s * 1e6,
+              "algorithmic_per_launch": dbytes}
+    dominant, other = (roof_d, roof_p) if d_ms_tot >= p_ms_tot else (roof_p, roof_d)
+    clocks = sampler.summary(t_wall0, t_wall1)
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = measure_e2e(args, pp, dp, dev, stream, attn, ws, world)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(pp, dp, args.cpu_seconds)
+
+    line = {
+        "metric": METRIC, "value": tflops, "unit": "TFLOP/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"{PREFILL_WL} + {DECODE_WL}",
+                   "prefill": "causal bf16 B=1 Hq=32 Hkv=8 Sq=Sk=2048 d=128 paged bs=64 permuted",
+                   "decode": "bf16 B=64 Hq=32 Hkv=8 d=128 Sk~U[512,8192] paged bs=16 splits=8",
+                   "l2": "flushed before every step (256 MiB write)",
+                   "parallelism": f"replica x{world}" if world > 1 else "single GPU"},
+        "decode": {"value": gbs, "unit": "GB/s", "frac_of_hbm": gbs / world / peaks["hbm_gbs"],
+                   "bytes_per_step": dbytes, "ms_per_call": d_avg_s * 1e3},
+        "prefill": {"value": tflops, "unit": "TFLOP/s",
+                    "frac_of_bf16": tflops / world / peaks["bf16_tflops"],
+                    "flops_per_step": flops, "ms_per_call": p_avg_s * 1e3},
+        "roofline": dominant, "roofline_other": other,
+        "gpu_launches": K * 3,
+        "clocks": clocks,
+        "e2e": e2e,
+        "cpu_baseline": cpu,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def measure_e2e(args, pp, dp, dev, stream, attn, ws, world):
+    """Host buffers through the public API: copy inputs in, run, copy outputs out."""
+    host_p = {k: getattr(pp, k).pin_memory() for k in ("q", "k_cache", "v_cache", "block_table",
+                                                       "query_start_loc", "seq_lens")}
+    host_d = {k: getattr(dp, k).pin_memory() for k in ("q", "k_cache", "v_cache", "block_table",
+                                                       "query_start_loc", "seq_lens")}
+    dev_p = {k: torch.empty_like(v, device=dev) for k, v in host_p.items()}
+    dev_d = {k: torch.empty_like(v, device=dev) for k, v in host_d.items()}
+    p_out = torch.empty_like(dev_p["q"])
+    d_out = torch.empty_like(dev_d["q"])
+    p_host_out = torch.empty_like(host_p["q"]).pin_memory()
+    d_host_out = torch.empty_like(host_d["q"]).pin_memory()
+    h2d_p = sum(v.numel() * v.element_size() for v in host_p.values())
+    h2d_d = sum(v.numel() * v.element_size() for v in host_d.values())
+    d2h_p = p_host_out.numel() * 2
+    d2h_d = d_host_out.numel() * 2
+
+    def step(ev):
+        ev[0].record(stream)
+        for k in dev_p:
+            dev_p[k].copy_(host_p[k], non_blocking=True)
+        attn.attn_fwd_prefill(p_out, dev_p["q"], dev_p["k_cache"], dev_p["v_cache"],
+                              dev_p["block_table"], dev_p["query_start_loc"], dev_p["seq_lens"],
+                              max_seqlen_q=pp.max_seqlen_q, max_seqlen_k=pp.max_seqlen_k,
+                              scale=pp.scale, causal=True, stream=stream)
+        p_host_out.copy_(p_out, non_blocking=True)
+        ev[1].record(stream)
+        for k in dev_d:
+            dev_d[k].copy_(host_d[k], non_blocking=True)
+        attn.attn_fwd_decode(d_out, dev_d["q"], dev_d["k_cache"], dev_d["v_cache"],
+                             dev_d["block_table"], dev_d["seq_lens"], max_seqlen_k=dp.max_seqlen_k,
+                             scale=dp.scale, num_splits=DECODE_SPLITS, workspace=ws, stream=stream)
+        d_host_out.copy_(d_out, non_blocking=True)
+        ev[2].record(stream)
+
+    n = max(3, min(args.steps, args.e2e_steps))
+    for _ in range(2):
+        step([torch.cuda.Event(enable_timing=True) for _ in range(3)])
+    torch.cuda.synchronize(dev)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n)]
+    barrier(world)
+    for e in evs:
+        step(e)
+    torch.cuda.synchronize(dev)
+    p_ms = sum(e[0].elapsed_time(e[1]) for e in evs)
+    d_ms = sum(e[1].elapsed_time(e[2]) for e in evs)
+    p_ms, d_ms = max_over_ranks(world, dev, [p_ms, d_ms])
+    flops = prefill_flops(pp)
+    return {"value": world * flops * n / (p_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+            "h2d_bytes_per_step": h2d_p + h2d_d, "d2h_bytes_per_step": d2h_p + d2h_d,
+            "steps": n,
+            "decode": {"value": world * decode_bytes(dp) * n / (d_ms * 1e-3) / 1e9, "unit": "GB/s"},
+            "note": "prefill part: H2D of its inputs + kernel + D2H of O; decode part likewise"}
+
+
+# ----------------------------------------------------------------------------
+# the oracle (CPU baseline and reference arm)
+# ----------------------------------------------------------------------------
+
+def oracle_sample(prob, n_rows, seed):
+    rng = np.random.default_rng(seed)
+    total = prob.total_q * prob.num_q_heads
+    return np.sort(rng.choice(total, size=min(n_rows, total), replace=False)).astype(np.int64)
+
+
+def oracle_cost(prob, rows):
+    """Unmasked FLOPs of the sampled rows (same count as the GPU metric)."""
+    H = prob.num_q_heads
+    qsl = prob.query_start_loc.numpy()
+    tok = rows // H
+    b = np.searchsorted(qsl, tok, side="right") - 1
+    i = tok - qsl[b]
+    sq = qsl[b + 1] - qsl[b]
+    sk = np.asarray(prob.kv_lens)[b]
+    vis = np.minimum(sk, i + (sk - sq) + 1) if prob.causal else sk
+    return 4.0 * prob.head_size * float(np.clip(vis, 0, None).sum())
+
+
+def oracle_bytes(prob, rows):
+    """K/V bytes the sampled decode rows read, scaled like the GPU metric
+    (one K/V read per kv head shared by its group)."""
+    H, G = prob.num_q_heads, prob.num_q_heads // prob.num_kv_heads
+    tok = rows // H
+    sk = np.asarray(prob.kv_lens)[tok]
+    per_row = sk * prob.head_size * 2 * 2 / G + 2 * prob.head_size * 2
+    return float(per_row.sum())
+
+
+def time_oracle(prob, rows, threads):
+    from oracle import oracle
+    t0 = time.perf_counter()
+    oracle.sdpa(prob.q, prob.k_cache, prob.v_cache, prob.block_table, prob.query_start_loc,
+                prob.seq_lens, num_q_heads=prob.num_q_heads, num_kv_heads=prob.num_kv_heads,
+                head_size=prob.head_size, block_size=prob.block_size, scale=prob.scale,
+                causal=prob.causal, dtype=oracle.BF16, rows=rows, n_threads=threads,
+                want_lse=False)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(pp, dp, seconds):
+    threads = os.cpu_count() or 1
+    # calibrate on a small sample, then size the sample for ~seconds/2 each
+    r0 = oracle_sample(pp, 256, 7)
+    t0 = time_oracle(pp, r0, threads)
+    n_p = int(max(256, min(pp.total_q * pp.num_q_heads, 256 * (seconds / 2) / max(t0, 1e-3))))
+    rp = oracle_sample(pp, n_p, 8)
+    tp = time_oracle(pp, rp, threads)
+    rd0 = oracle_sample(dp, 64, 9)
+    td0 = time_oracle(dp, rd0, threads)
+    n_d = int(max(64, min(dp.total_q * dp.num_q_heads, 64 * (seconds / 2) / max(td0, 1e-3))))
+    rd = oracle_sample(dp, n_d, 10)
+    td = time_oracle(dp, rd, threads)
+    return {"value": oracle_cost(pp, rp) / tp / 1e12, "unit": "TFLOP/s", "cores": threads,
+            "kind": "oracle",
+            "sample": f"prefill: {len(rp)} random (token, head) rows of {PREFILL_WL} in {tp:.1f}s; "
+                      f"decode: {len(rd)} rows of {DECODE_WL} in {td:.1f}s",
+            "decode": {"value": oracle_bytes(dp, rd) / td / 1e9, "unit": "GB/s"}}
+
+
+def run_reference(args, rank, world):
+    """Reference arm: the fp64 oracle on the host cores, each step a bounded
+    row sample of the same two workloads."""
+    if rank != 0:
+        return
+    pp, dp = make_problems(seed=0)
+    threads = os.cpu_count() or 1
+    rows_p = oracle_sample(pp, args.ref_rows, 11)
+    rows_d = oracle_sample(dp, max(16, args.ref_rows // 4), 12)
+    for _ in range(args.warmup):
+        time_oracle(pp, rows_p, threads)
+        time_oracle(dp, rows_d, threads)
+    tp = td = 0.0
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        tp += time_oracle(pp, rows_p, threads)
+        td += time_oracle(dp, rows_d, threads)
+    wall = time.perf_counter() - t0
+    K = args.steps
+    value = oracle_cost(pp, rows_p) * K / tp / 1e12
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": wall / K * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "impl": "reference",
+        "config": {"workload": f"{PREFILL_WL} + {DECODE_WL}",
+                   "sample": f"{len(rows_p)} prefill rows + {len(rows_d)} decode rows per step"},
+        "decode": {"value": oracle_bytes(dp, rows_d) * K / td / 1e9, "unit": "GB/s"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                         "sample": f"{len(rows_p)} random prefill rows + {len(rows_d)} decode "
+                                   f"rows per step"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------
+# distributed plumbing
+# ----------------------------------------------------------------------------
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(world, dev, vals):
+    if world == 1:
+        return vals
+    import torch.distributed as dist
+    t = torch.tensor(vals, dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=16.0)
+    ap.add_argument("--ref-rows", type=int, default=128)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if world > 1:
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group("nccl", device_id=dev)
+    try:
+        run_ours(args, rank, world, dev)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,161 @@
+/*
+ * attn_fwd.h -- C ABI of the GB300 (sm_103a) fused scaled-dot-product-attention
+ * forward library (libattn_fwd_sm103.so).
+ *
+ * What it computes.  For every sequence b, query head h and query row i:
+ *     O[i, h, :] = sum_j softmax_j(tau * <Q[i, h, :], K[j, kvh, :]>) V[j, kvh, :]
+ * over the visible keys j, with kvh = h / (num_q_heads / num_kv_heads).  This
+ * is the specification of "gfx942 unified attention, from the math up",
+ * sec. 1, evaluated by the online-softmax recurrence of sec. 3 (running max m,
+ * denominator l, rescale alpha = e^(m_old - m_new), un-normalised o, final
+ * o / l) without ever forming the query-by-key score matrix.  Keys are read
+ * from a paged cache through a block table (sec. 5); GQA groups follow the
+ * repeat_interleave convention of sec. 5 and sec. 10.  Causal masking is
+ * bottom-right aligned (sec. 4, and the "Troubleshooting" section of
+ * "gfx942 unified attention - parity + benchmark harness"): row i of a
+ * sequence with query length Sq and kv length Sk sees keys j <= i + Sk - Sq.
+ * A row that sees no key (causal with Sq > Sk, or Sk = 0) gets O = 0 and
+ * log-sum-exp -inf.  Output rounding modes are those of "MoonMath.ai abre un
+ * nucleo de atencion HIP para AMD MI300X ..." (7minutos.es), section "Punto de
+ * referencia": RTNE, RTNA (ties away from zero) and RTZ.
+ *
+ * Memory and threading rules for every entry point:
+ *   - Every pointer argument is caller-owned DEVICE memory unless stated
+ *     otherwise; tensors are dense, row-major, with the shapes given.  The
+ *     library never allocates or frees device memory and keeps no pointer
+ *     after the call returns.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL is the legacy
+ *     default stream).  Inputs must stay valid until the work completes.
+ *   - Argument errors are detected on the host and returned before anything
+ *     is launched.  A failed launch returns ATTN_ERR_CUDA.  Errors that can
+ *     only be seen on the device (a block-table entry outside [0, num_blocks),
+ *     a sequence longer than max_seqlen_*, a wait that timed out) are written
+ *     to *status_dev when it is non-NULL (first error wins; the caller sets it
+ *     to 0 beforehand and reads it after synchronising); the offending work is
+ *     skipped or loads zeros, never reads outside the given tensors.
+ *   - Nothing throws across the ABI.  The library requires a compute
+ *     capability 10.3 (sm_103) device; otherwise ATTN_ERR_UNSUPPORTED.
+ */
+#ifndef ATTN_FWD_H_
+#define ATTN_FWD_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  ATTN_OK = 0,
+  ATTN_ERR_INVALID_ARG = 1,   /* bad pointer, size or enum value */
+  ATTN_ERR_UNSUPPORTED = 2,   /* valid request outside the compiled set */
+  ATTN_ERR_CUDA = 3,          /* a CUDA call or launch failed */
+  ATTN_ERR_WORKSPACE = 4,     /* workspace missing, too small or misaligned */
+  ATTN_ERR_BAD_BLOCK_TABLE = 5, /* (device status only) page id out of range */
+  ATTN_ERR_TIMEOUT = 6        /* (device status only) a pipeline wait timed out */
+} attn_status_t;
+
+typedef enum { ATTN_F16 = 0, ATTN_BF16 = 1 } attn_dtype_t;
+
+/* Output rounding: RTNE = nearest, ties to even; RTNA = nearest, ties away
+ * from zero; RTZ = toward zero.  ATTN_OUT_F32 writes the fp32 value o / l
+ * unrounded (out is then float*). */
+typedef enum { ATTN_RTNE = 0, ATTN_RTNA = 1, ATTN_RTZ = 2, ATTN_OUT_F32 = 3 } attn_round_t;
+
+/*
+ * attn_fwd_prefill -- prefill / dense forward over packed queries and a paged
+ * KV cache ("gfx942 unified attention, from the math up", sec. 3-5).
+ *
+ *   out          [total_q, num_q_heads, head_size], dtype (fp32 for ATTN_OUT_F32)
+ *   q            [total_q, num_q_heads, head_size], dtype; 16-byte aligned
+ *   k_cache      [num_blocks, block_size, num_kv_heads, head_size], dtype; 16-byte aligned
+ *   v_cache      same shape as k_cache
+ *   block_table  [num_seqs, block_table_stride] int32: page ids of each
+ *                sequence's keys in order (key j of sequence b lives in page
+ *                block_table[b][j / block_size], slot j % block_size); only
+ *                the first ceil(seq_lens[b] / block_size) entries are read.
+ *   query_start_loc [num_seqs + 1] int32: prefix sum of query lengths;
+ *                sequence b owns rows [query_start_loc[b], query_start_loc[b+1]).
+ *   seq_lens     [num_seqs] int32: kv length of each sequence.
+ *   max_seqlen_q / max_seqlen_k: upper bounds of the per-sequence lengths
+ *                (used to size the grid; violations are reported on the device).
+ *   head_size    64 or 128.  block_size: a multiple of 16 that divides 128,
+ *                or a multiple of 128.  num_q_heads % num_kv_heads == 0.
+ *   scale        tau (> 0), normally 1/sqrt(head_size).
+ *   causal       0 or 1 (bottom-right aligned).
+ *   lse_out      optional [total_q, num_q_heads] fp32 natural-log log-sum-exp
+ *                of each row's scaled scores, or NULL.
+ *   status_dev   optional device int32 status word, or NULL.
+ *   stream       cudaStream_t.
+ * Dense BSHD input [B, S, H, d] is the special case query_start_loc =
+ * {0, S, 2S, ...}, block_size = S, num_blocks = B, block_table[b] = {b}.
+ */
+attn_status_t attn_fwd_prefill(void* out, const void* q, const void* k_cache, const void* v_cache,
+                               const int32_t* block_table, int32_t block_table_stride,
+                               const int32_t* query_start_loc, const int32_t* seq_lens,
+                               int32_t num_seqs, int32_t max_seqlen_q, int32_t max_seqlen_k,
+                               int32_t total_q, int32_t num_q_heads, int32_t num_kv_heads,
+                               int32_t head_size, int32_t block_size, int32_t num_blocks,
+                               float scale, int32_t causal, attn_dtype_t dtype,
+                               attn_round_t rounding, float* lse_out, int32_t* status_dev,
+                               void* stream);
+
+/*
+ * attn_decode_workspace_size -- bytes of device workspace attn_fwd_decode
+ * needs for these sizes (0 when num_splits == 1).  Pure host arithmetic.
+ */
+size_t attn_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t head_size,
+                                  int32_t num_splits);
+
+/*
+ * attn_fwd_decode -- one query row per sequence attending to all of its
+ * kv_len keys (decode: causal and non-causal coincide for a single query,
+ * "gfx942 unified attention, from the math up", sec. 4), by the split-KV
+ * scheme of sec. 8: the keys of each sequence are cut into num_splits
+ * contiguous parts of ceil(ceil(kv_len / num_splits) / 16) * 16 keys, each
+ * part reduced to a partial softmax state in the workspace, and the parts
+ * merged by the log-sum-exp rule.
+ *
+ *   out          [num_seqs, num_q_heads, head_size], dtype (fp32 for ATTN_OUT_F32)
+ *   q            [num_seqs, num_q_heads, head_size], dtype
+ *   k_cache, v_cache, block_table, block_table_stride, seq_lens,
+ *   num_q_heads, num_kv_heads, head_size, block_size, num_blocks, scale:
+ *                as for attn_fwd_prefill, except that block_size only needs
+ *                to be a multiple of 16.
+ *   num_splits   1 .. 64.
+ *   lse_out      optional [num_seqs, num_q_heads] fp32, or NULL.
+ *   workspace    device memory of at least attn_decode_workspace_size(...)
+ *                bytes, 16-byte aligned (may be NULL when num_splits == 1);
+ *                owned by the caller, overwritten by the call, and must not
+ *                be shared by calls that overlap on the device.
+ */
+attn_status_t attn_fwd_decode(void* out, const void* q, const void* k_cache, const void* v_cache,
+                              const int32_t* block_table, int32_t block_table_stride,
+                              const int32_t* seq_lens, int32_t num_seqs, int32_t max_seqlen_k,
+                              int32_t num_q_heads, int32_t num_kv_heads, int32_t head_size,
+                              int32_t block_size, int32_t num_blocks, float scale,
+                              int32_t num_splits, attn_dtype_t dtype, attn_round_t rounding,
+                              float* lse_out, void* workspace, size_t workspace_bytes,
+                              int32_t* status_dev, void* stream);
+
+/*
+ * attn_round_f32 -- applies the output rounding of the epilogues to n fp32
+ * values: out[i] = round(in[i]) as bf16 or fp16 bit patterns (uint16_t[n]),
+ * rounding in {ATTN_RTNE, ATTN_RTNA, ATTN_RTZ}.  Exposed so that the rounding
+ * can be checked on its own.
+ */
+attn_status_t attn_round_f32(void* out, const float* in, int64_t n, attn_dtype_t dtype,
+                             attn_round_t rounding, void* stream);
+
+/* Human-readable name of a status code (static string). */
+const char* attn_status_string(attn_status_t status);
+
+/* ABI version of this header (incremented on incompatible changes). */
+int32_t attn_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_FWD_H_ */

@@ -1,0 +1,159 @@
+"""Host-side checks of the C ABI (no GPU needed, nothing is launched).
+
+  - the shared library builds, loads and exports every function that
+    include/attn_fwd.h declares;
+  - argument errors are returned before any CUDA call (so they work on a
+    machine without a GPU): null pointers, head-group mismatch, head sizes and
+    block sizes outside the compiled set, bad enums, bad scale, short block
+    table, missing workspace;
+  - the workspace size is plain arithmetic;
+  - the Python binding refuses CPU tensors and wrong dtypes instead of
+    falling back to anything.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER_DIR = os.path.join(ROOT, "include")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from attention_forward_sdpa_gb300 import build_ext
+    import attention_forward_sdpa_gb300 as pkg
+    build_ext.build()
+    return pkg.load_library()
+
+
+def declared_functions():
+    names = []
+    for f in sorted(os.listdir(HEADER_DIR)):
+        if not f.endswith(".h"):
+            continue
+        text = open(os.path.join(HEADER_DIR, f)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"^\s*[A-Za-z_][\w\s\*]*?\b(attn_\w+)\s*\(", text, flags=re.M):
+            names.append(m.group(1))
+    return sorted(set(names))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ("attn_fwd_prefill", "attn_fwd_decode", "attn_decode_workspace_size",
+              "attn_round_f32", "attn_status_string", "attn_abi_version"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+        assert ctypes.cast(getattr(lib, name), ctypes.c_void_p).value
+
+
+def test_status_strings_and_version(lib):
+    assert lib.attn_abi_version() == 1
+    for code in range(7):
+        assert lib.attn_status_string(code)
+    assert lib.attn_status_string(99) == b"unknown status"
+
+
+def test_workspace_size_is_arithmetic(lib):
+    assert lib.attn_decode_workspace_size(64, 32, 128, 8) == 64 * 32 * 8 * (128 + 2) * 4
+    assert lib.attn_decode_workspace_size(64, 32, 128, 1) == 0
+    assert lib.attn_decode_workspace_size(0, 32, 128, 8) == 0
+
+
+FAKE = ctypes.c_void_p(0x10000)  # never dereferenced: validation fails first
+
+
+def prefill_args(**over):
+    a = dict(out=FAKE, q=FAKE, k=FAKE, v=FAKE, bt=FAKE, bt_stride=4, qsl=FAKE, sl=FAKE,
+             num_seqs=2, max_q=100, max_k=200, total_q=150, hq=8, hkv=2, d=128, bs=64, nb=10,
+             scale=0.088, causal=1, dtype=1, rounding=0, lse=None, status=None, stream=None)
+    a.update(over)
+    return [a[k] for k in ("out", "q", "k", "v", "bt", "bt_stride", "qsl", "sl", "num_seqs",
+                           "max_q", "max_k", "total_q", "hq", "hkv", "d", "bs", "nb", "scale",
+                           "causal", "dtype", "rounding", "lse", "status", "stream")]
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(q=None), 1),
+    (dict(out=None), 1),
+    (dict(bt=None), 1),
+    (dict(hq=6, hkv=4), 1),
+    (dict(hkv=0), 1),
+    (dict(d=96), 2),
+    (dict(d=256), 2),
+    (dict(bs=48), 2),
+    (dict(bs=8), 2),
+    (dict(bs=192), 2),
+    (dict(dtype=7), 1),
+    (dict(rounding=9), 1),
+    (dict(causal=2), 1),
+    (dict(scale=0.0), 1),
+    (dict(scale=float("nan")), 1),
+    (dict(bt_stride=3), 1),
+    (dict(num_seqs=-1), 1),
+    (dict(q=ctypes.c_void_p(0x10008)), 1),
+])
+def test_prefill_rejects_bad_arguments(lib, over, code):
+    assert lib.attn_fwd_prefill(*prefill_args(**over)) == code
+
+
+def test_prefill_empty_problem_is_a_no_op(lib):
+    assert lib.attn_fwd_prefill(*prefill_args(num_seqs=0)) == 0
+    assert lib.attn_fwd_prefill(*prefill_args(total_q=0)) == 0
+
+
+def decode_args(**over):
+    a = dict(out=FAKE, q=FAKE, k=FAKE, v=FAKE, bt=FAKE, bt_stride=512, sl=FAKE, num_seqs=64,
+             max_k=8192, hq=32, hkv=8, d=128, bs=16, nb=100000, scale=0.088, splits=8, dtype=1,
+             rounding=0, lse=None, ws=FAKE, ws_bytes=64 * 32 * 8 * 130 * 4, status=None,
+             stream=None)
+    a.update(over)
+    return [a[k] for k in ("out", "q", "k", "v", "bt", "bt_stride", "sl", "num_seqs", "max_k",
+                           "hq", "hkv", "d", "bs", "nb", "scale", "splits", "dtype", "rounding",
+                           "lse", "ws", "ws_bytes", "status", "stream")]
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(q=None), 1),
+    (dict(sl=None), 1),
+    (dict(hq=30), 1),
+    (dict(d=80), 2),
+    (dict(bs=24), 2),
+    (dict(splits=0), 1),
+    (dict(splits=65), 1),
+    (dict(bt_stride=511), 1),
+    (dict(ws=None), 4),
+    (dict(ws_bytes=100), 4),
+    (dict(ws=ctypes.c_void_p(0x10004)), 4),
+    (dict(rounding=4), 1),
+])
+def test_decode_rejects_bad_arguments(lib, over, code):
+    assert lib.attn_fwd_decode(*decode_args(**over)) == code
+
+
+def test_round_rejects_bad_arguments(lib):
+    assert lib.attn_round_f32(FAKE, FAKE, -1, 1, 0, None) == 1
+    assert lib.attn_round_f32(FAKE, FAKE, 10, 1, 3, None) == 1
+    assert lib.attn_round_f32(None, FAKE, 10, 1, 0, None) == 1
+    assert lib.attn_round_f32(FAKE, FAKE, 0, 1, 0, None) == 0
+
+
+def test_binding_refuses_cpu_tensors(lib):
+    import attention_forward_sdpa_gb300 as attn
+    q = torch.zeros(4, 2, 64, dtype=torch.bfloat16)
+    k = torch.zeros(1, 16, 2, 64, dtype=torch.bfloat16)
+    bt = torch.zeros(1, 1, dtype=torch.int32)
+    with pytest.raises(ValueError):
+        attn.attn_fwd_prefill(torch.empty_like(q), q, k, k, bt, torch.tensor([0, 4], dtype=torch.int32),
+                              torch.tensor([4], dtype=torch.int32), max_seqlen_q=4, max_seqlen_k=4,
+                              scale=0.125, causal=True)
+    with pytest.raises(TypeError):
+        attn.prefill(q.float(), k, k, bt, torch.tensor([0, 4], dtype=torch.int32),
+                     torch.tensor([4], dtype=torch.int32), max_seqlen_q=4, max_seqlen_k=4)
