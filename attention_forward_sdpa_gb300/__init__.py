@@ -8,7 +8,7 @@ kernels; there is no fallback of any kind.  If the library has not been built
 (``python -m attention_forward_sdpa_gb300.build_ext``) every call raises.
 
 Entry points (same names as the C functions):
-  attn_fwd_prefill, attn_fwd_decode, attn_decode_workspace_size,
+  attn_fwd_prefill, attn_fwd_decode, attn_fwd_decode_noalloc, attn_decode_workspace_size,
   attn_round_f32, attn_status_string, attn_abi_version
 and allocating conveniences ``prefill`` and ``decode`` that create the output
 (and the decode workspace) with torch on the inputs' device.
@@ -23,7 +23,8 @@ import torch
 
 from .build_ext import LIB_PATH
 
-__all__ = ["attn_fwd_prefill", "attn_fwd_decode", "attn_decode_workspace_size",
+__all__ = ["attn_fwd_prefill", "attn_fwd_decode", "attn_fwd_decode_noalloc",
+           "attn_decode_workspace_size",
            "attn_round_f32", "attn_status_string", "attn_abi_version", "prefill", "decode",
            "AttnError", "library_path", "load_library", "RTNE", "RTNA", "RTZ", "OUT_F32"]
 
@@ -70,6 +71,10 @@ def load_library() -> ctypes.CDLL:
         lib.attn_fwd_decode.restype = ctypes.c_int
         lib.attn_fwd_decode.argtypes = [P, P, P, P, P, i32, P, i32, i32, i32, i32, i32, i32, i32,
                                         f32, i32, ctypes.c_int, ctypes.c_int, P, P, sz, P, P]
+        lib.attn_fwd_decode_noalloc.restype = ctypes.c_int
+        lib.attn_fwd_decode_noalloc.argtypes = [P, P, P, P, P, i32, P, i32, i32, i32, i32, i32,
+                                                i32, i32, f32, i32, ctypes.c_int, ctypes.c_int, P,
+                                                P, P]
         lib.attn_round_f32.restype = ctypes.c_int
         lib.attn_round_f32.argtypes = [P, P, i64, ctypes.c_int, ctypes.c_int, P]
         lib.attn_status_string.restype = ctypes.c_char_p
@@ -206,6 +211,39 @@ def attn_fwd_decode(out, q, k_cache, v_cache, block_table, seq_lens, *, max_seql
                              _ptr(lse), _ptr(workspace), ws_bytes, _ptr(status),
                              _stream_handle(stream))
     _check(rc, "attn_fwd_decode")
+
+
+def attn_fwd_decode_noalloc(out, q, k_cache, v_cache, block_table, seq_lens, *,
+                            max_seqlen_k: int, scale: float, num_splits: int,
+                            rounding: int = RTNE, lse=None, status=None, stream=None) -> None:
+    """Calls attn_fwd_decode_noalloc: the decode without a caller workspace, for
+    callers that may not allocate device memory (the split partials live in a
+    library-owned device array of ATTN_DECODE_NOALLOC_SCRATCH_BYTES; calls on
+    one device must not overlap)."""
+    lib = load_library()
+    dt = _dtype_code(q.dtype)
+    _dev(q, "q")
+    _dev(k_cache, "k_cache", q.dtype)
+    _dev(v_cache, "v_cache", q.dtype)
+    _dev(out, "out", torch.float32 if rounding == OUT_F32 else q.dtype)
+    _dev(block_table, "block_table", torch.int32)
+    _dev(seq_lens, "seq_lens", torch.int32)
+    if lse is not None:
+        _dev(lse, "lse", torch.float32)
+    if status is not None:
+        _dev(status, "status", torch.int32)
+    num_seqs, hq, d = q.shape
+    nb, bs, hkv, d2 = k_cache.shape
+    if d2 != d or tuple(v_cache.shape) != tuple(k_cache.shape) or tuple(out.shape) != tuple(q.shape):
+        raise ValueError("inconsistent q / k_cache / v_cache / out shapes")
+    if seq_lens.shape[0] != num_seqs or block_table.dim() != 2 or block_table.shape[0] != num_seqs:
+        raise ValueError("inconsistent block_table / seq_lens shapes")
+    rc = lib.attn_fwd_decode_noalloc(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache),
+                                     _ptr(block_table), block_table.shape[1], _ptr(seq_lens),
+                                     num_seqs, int(max_seqlen_k), hq, hkv, d, bs, nb, float(scale),
+                                     int(num_splits), dt, int(rounding), _ptr(lse), _ptr(status),
+                                     _stream_handle(stream))
+    _check(rc, "attn_fwd_decode_noalloc")
 
 
 def attn_round_f32(out, x, *, dtype: torch.dtype, rounding: int, stream=None) -> None:

@@ -139,6 +139,43 @@ attn_status_t attn_fwd_decode(void* out, const void* q, const void* k_cache, con
                               float* lse_out, void* workspace, size_t workspace_bytes,
                               int32_t* status_dev, void* stream);
 
+/* Size of the device scratch array built into the library for
+ * attn_fwd_decode_noalloc (16 MiB on every GPU that loads the library). */
+#define ATTN_DECODE_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
+
+/*
+ * attn_fwd_decode_noalloc -- attn_fwd_decode for callers that may not
+ * allocate device memory.  The paper has no counterpart of this entry point;
+ * it exists for this library's users.  A latency-critical serving loop cannot call
+ * cudaMalloc (it may synchronise the device and has unbounded cost), and a
+ * host framework whose allocator owns all device memory, or a plugin that
+ * only receives input and output pointers, has no way to supply a workspace.
+ * This entry point takes the same arguments as attn_fwd_decode minus the
+ * workspace, runs the same kernels, and keeps the split partials in a
+ * library-owned device array of ATTN_DECODE_NOALLOC_SCRATCH_BYTES.
+ *
+ *   - It allocates nothing: no cudaMalloc, cudaFree or allocating library call.
+ *   - Problems whose split partials need more than the array, i.e. with
+ *     attn_decode_workspace_size(num_seqs, num_q_heads, head_size, num_splits)
+ *     > ATTN_DECODE_NOALLOC_SCRATCH_BYTES, are rejected with
+ *     ATTN_ERR_WORKSPACE before anything is launched.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress with that device current) and caches it; make
+ *     that first call before any stream capture.
+ *   - All calls on a device share the array.  Each call writes every partial
+ *     it reads, so nothing needs clearing, but calls that may overlap on the
+ *     device (unordered streams) race and must not be issued.
+ *   - Other arguments, errors and the status word: as for attn_fwd_decode.
+ */
+attn_status_t attn_fwd_decode_noalloc(void* out, const void* q, const void* k_cache,
+                                      const void* v_cache, const int32_t* block_table,
+                                      int32_t block_table_stride, const int32_t* seq_lens,
+                                      int32_t num_seqs, int32_t max_seqlen_k, int32_t num_q_heads,
+                                      int32_t num_kv_heads, int32_t head_size, int32_t block_size,
+                                      int32_t num_blocks, float scale, int32_t num_splits,
+                                      attn_dtype_t dtype, attn_round_t rounding, float* lse_out,
+                                      int32_t* status_dev, void* stream);
+
 /*
  * attn_round_f32 -- applies the output rounding of the epilogues to n fp32
  * values: out[i] = round(in[i]) as bf16 or fp16 bit patterns (uint16_t[n]),
