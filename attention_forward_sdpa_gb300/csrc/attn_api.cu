@@ -49,9 +49,17 @@ attn_status_t check_device() {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-bool encode(CUtensorMap* map, bool bf16, int rank, const cuuint64_t* dims,
-            const cuuint64_t* strides_bytes, const cuuint32_t* box, const void* base,
-            CUtensorMapSwizzle swz) {
+bool valid_scale(float s) { return std::isfinite(s) && s > 0.f; }
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+}  // namespace
+
+namespace attn {
+
+bool encode_tiled(CUtensorMap* map, bool bf16, int rank, const cuuint64_t* dims,
+                  const cuuint64_t* strides_bytes, const cuuint32_t* box, const void* base,
+                  CUtensorMapSwizzle swz) {
   EncodeTiledFn fn = get_encode_fn();
   if (!fn) return false;
   cuuint32_t estr[5] = {1, 1, 1, 1, 1};
@@ -61,11 +69,73 @@ bool encode(CUtensorMap* map, bool bf16, int rank, const cuuint64_t* dims,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-bool valid_scale(float s) { return std::isfinite(s) && s > 0.f; }
+int device_sm_count() {
+  static int cached[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (cached[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
 
-constexpr float kLog2e = 1.4426950408889634f;
+// Workspace: [partial o: rows * splits * d fp32][partial (m, l): rows * splits
+// * 2 fp32][work counter, 256 bytes].
+int decode_prepare_and_launch(DecodeParams& p, int head_size, bool bf16, void* workspace,
+                              cudaStream_t stream) {
+  const size_t rows = (size_t)p.num_seqs * (size_t)p.num_q_heads * (size_t)p.num_splits;
+  float* ws = static_cast<float*>(workspace);
+  if (p.num_splits > 1) {
+    p.part_o = ws;
+    p.part_ml = ws + rows * (size_t)head_size;
+    p.counter = reinterpret_cast<int32_t*>(p.part_ml + rows * 2);
+  } else {
+    p.part_o = nullptr;
+    p.part_ml = nullptr;
+    p.counter = reinterpret_cast<int32_t*>(ws);
+  }
+  const int G = p.num_q_heads / p.num_kv_heads;
+  const bool tc_path = head_size == 128 && (G <= 16 || G % 16 == 0);
+  if (!tc_path) {
+    cudaError_t e = launch_decode(p, head_size, bf16, G, stream);
+    return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+  }
+  p.heads_per_item = G <= 16 ? G : 16;
+  p.q_box_rows = p.num_q_heads < 16 ? p.num_q_heads : 16;
+  const int64_t n_items =
+      (int64_t)p.num_seqs * (p.num_q_heads / p.heads_per_item) * (int64_t)p.num_splits;
+  if (n_items > 2147483647) return ATTN_ERR_UNSUPPORTED;
+  p.n_items = (int32_t)n_items;
+  const cuuint64_t d = (cuuint64_t)head_size;
+  {
+    const cuuint64_t dims[3] = {d, (cuuint64_t)p.num_q_heads, (cuuint64_t)p.num_seqs};
+    const cuuint64_t strides[2] = {d * 2, d * 2 * (cuuint64_t)p.num_q_heads};
+    const cuuint32_t box[3] = {64, (cuuint32_t)p.q_box_rows, 1};
+    if (!encode_tiled(&p.tm_q, bf16, 3, dims, strides, box, p.q, CU_TENSOR_MAP_SWIZZLE_128B))
+      return ATTN_ERR_CUDA;
+  }
+  {
+    const cuuint64_t dims[4] = {d, (cuuint64_t)p.num_kv_heads, (cuuint64_t)p.block_size,
+                                (cuuint64_t)p.num_blocks};
+    const cuuint64_t strides[3] = {d * 2, d * 2 * (cuuint64_t)p.num_kv_heads,
+                                   d * 2 * (cuuint64_t)p.num_kv_heads * (cuuint64_t)p.block_size};
+    const cuuint32_t box[4] = {64, 1, 16, 1};
+    if (!encode_tiled(&p.tm_k, bf16, 4, dims, strides, box, p.k_cache, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_tiled(&p.tm_v, bf16, 4, dims, strides, box, p.v_cache, CU_TENSOR_MAP_SWIZZLE_128B))
+      return ATTN_ERR_CUDA;
+  }
+  const int sms = device_sm_count();
+  if (sms <= 0) return ATTN_ERR_CUDA;
+  const int grid = (int)(n_items < sms ? n_items : sms);
+  if (cudaMemsetAsync(p.counter, 0, sizeof(int32_t), stream) != cudaSuccess) return ATTN_ERR_CUDA;
+  cudaError_t e = launch_decode_tc(p, bf16, grid, stream);
+  if (e == cudaSuccess && p.num_splits > 1) e = launch_decode_combine(p, head_size, bf16, stream);
+  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
 
-}  // namespace
+}  // namespace attn
 
 extern "C" {
 
@@ -128,7 +198,7 @@ attn_status_t attn_fwd_prefill(void* out, const void* q, const void* k_cache, co
     const cuuint64_t dims[3] = {d, (cuuint64_t)num_q_heads, (cuuint64_t)total_q};
     const cuuint64_t strides[2] = {d * 2, d * 2 * (cuuint64_t)num_q_heads};
     const cuuint32_t box[3] = {64, 1, 128};
-    if (!encode(&p.tm_q, bf16, 3, dims, strides, box, q, CU_TENSOR_MAP_SWIZZLE_128B)) return ATTN_ERR_CUDA;
+    if (!attn::encode_tiled(&p.tm_q, bf16, 3, dims, strides, box, q, CU_TENSOR_MAP_SWIZZLE_128B)) return ATTN_ERR_CUDA;
   }
   {
     const cuuint64_t dims[4] = {d, (cuuint64_t)num_kv_heads, (cuuint64_t)block_size,
@@ -136,8 +206,8 @@ attn_status_t attn_fwd_prefill(void* out, const void* q, const void* k_cache, co
     const cuuint64_t strides[3] = {d * 2, d * 2 * (cuuint64_t)num_kv_heads,
                                    d * 2 * (cuuint64_t)num_kv_heads * (cuuint64_t)block_size};
     const cuuint32_t box[4] = {64, 1, (cuuint32_t)(block_size < 128 ? block_size : 128), 1};
-    if (!encode(&p.tm_k, bf16, 4, dims, strides, box, k_cache, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode(&p.tm_v, bf16, 4, dims, strides, box, v_cache, CU_TENSOR_MAP_SWIZZLE_128B))
+    if (!attn::encode_tiled(&p.tm_k, bf16, 4, dims, strides, box, k_cache, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !attn::encode_tiled(&p.tm_v, bf16, 4, dims, strides, box, v_cache, CU_TENSOR_MAP_SWIZZLE_128B))
       return ATTN_ERR_CUDA;
   }
   p.out = out;
@@ -168,9 +238,11 @@ attn_status_t attn_fwd_prefill(void* out, const void* q, const void* k_cache, co
 
 size_t attn_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t head_size,
                                   int32_t num_splits) {
-  if (num_seqs <= 0 || num_q_heads <= 0 || head_size <= 0 || num_splits <= 1) return 0;
+  if (num_seqs <= 0 || num_q_heads <= 0 || head_size <= 0 || num_splits <= 0) return 0;
+  const size_t counter_bytes = 256;
+  if (num_splits == 1) return counter_bytes;
   const size_t rows = (size_t)num_seqs * (size_t)num_q_heads * (size_t)num_splits;
-  return rows * (size_t)head_size * sizeof(float) + rows * 2 * sizeof(float);
+  return rows * (size_t)head_size * sizeof(float) + rows * 2 * sizeof(float) + counter_bytes;
 }
 
 attn_status_t attn_fwd_decode(void* out, const void* q, const void* k_cache, const void* v_cache,
@@ -197,8 +269,7 @@ attn_status_t attn_fwd_decode(void* out, const void* q, const void* k_cache, con
   const int64_t pages_needed = ((int64_t)max_seqlen_k + block_size - 1) / block_size;
   if (block_table_stride < 1 || block_table_stride < pages_needed) return ATTN_ERR_INVALID_ARG;
   const size_t need = attn_decode_workspace_size(num_seqs, num_q_heads, head_size, num_splits);
-  if (need > 0 && (!workspace || workspace_bytes < need || !aligned16(workspace)))
-    return ATTN_ERR_WORKSPACE;
+  if (!workspace || workspace_bytes < need || !aligned16(workspace)) return ATTN_ERR_WORKSPACE;
   if (num_seqs > 65535 || (int64_t)num_q_heads > 65535) return ATTN_ERR_UNSUPPORTED;
 
   attn_status_t st = check_device();
@@ -214,11 +285,6 @@ attn_status_t attn_fwd_decode(void* out, const void* q, const void* k_cache, con
   p.status = status_dev;
   p.block_table = block_table;
   p.seq_lens = seq_lens;
-  if (need > 0) {
-    const size_t rows = (size_t)num_seqs * num_q_heads * num_splits;
-    p.part_o = static_cast<float*>(workspace);
-    p.part_ml = p.part_o + rows * (size_t)head_size;
-  }
   p.bt_stride = block_table_stride;
   p.num_seqs = num_seqs;
   p.max_seqlen_k = max_seqlen_k;
@@ -229,9 +295,8 @@ attn_status_t attn_fwd_decode(void* out, const void* q, const void* k_cache, con
   p.num_splits = num_splits;
   p.rounding = (int32_t)rounding;
   p.scale_log2 = scale * kLog2e;
-  cudaError_t e = attn::launch_decode(p, head_size, dtype == ATTN_BF16, num_q_heads / num_kv_heads,
-                                      static_cast<cudaStream_t>(stream));
-  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+  return (attn_status_t)attn::decode_prepare_and_launch(p, head_size, dtype == ATTN_BF16, workspace,
+                                                        static_cast<cudaStream_t>(stream));
 }
 
 attn_status_t attn_round_f32(void* out, const float* in, int64_t n, attn_dtype_t dtype,

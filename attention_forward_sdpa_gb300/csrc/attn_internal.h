@@ -37,6 +37,13 @@ struct PrefillParams {
 };
 
 struct DecodeParams {
+  CUtensorMap tm_q;     // Q [num_seqs, Hq, d]: dims (d, Hq, num_seqs), box (64, min(16, Hq), 1)
+  CUtensorMap tm_k;     // K cache: dims (d, Hkv, bs, num_blocks), box (64, 1, 16, 1)
+  CUtensorMap tm_v;     // V cache: same
+  int32_t* counter;     // work counter of the persistent kernel (zeroed before the launch)
+  int32_t n_items;      // num_seqs * (Hq / heads_per_item) * num_splits
+  int32_t heads_per_item;
+  int32_t q_box_rows;
   const void* q;        // [num_seqs, Hq, d]
   const void* k_cache;  // [num_blocks, bs, Hkv, d]
   const void* v_cache;  // [num_blocks, bs, Hkv, d]
@@ -64,6 +71,22 @@ cudaError_t launch_prefill(const PrefillParams& p, int head_size, bool bf16, dim
                            cudaStream_t stream);
 cudaError_t launch_decode(const DecodeParams& p, int head_size, bool bf16, int group,
                           cudaStream_t stream);
+cudaError_t launch_decode_tc(const DecodeParams& p, bool bf16, int grid, cudaStream_t stream);
+cudaError_t launch_decode_combine(const DecodeParams& p, int head_size, bool bf16,
+                                  cudaStream_t stream);
+
+// Shared by the two decode entry points: fills the kernel parameters from
+// the (already validated) arguments, places the partials and the work
+// counter in `workspace` (attn_decode_workspace_size bytes), and launches.
+// Returns an attn_status_t value.
+int decode_prepare_and_launch(DecodeParams& p, int head_size, bool bf16, void* workspace,
+                              cudaStream_t stream);
+
+bool encode_tiled(CUtensorMap* map, bool bf16, int rank, const cuuint64_t* dims,
+                  const cuuint64_t* strides_bytes, const cuuint32_t* box, const void* base,
+                  CUtensorMapSwizzle swz);
+int device_sm_count();
+
 cudaError_t launch_round(void* out, const float* in, int64_t n, bool bf16, int mode,
                          cudaStream_t stream);
 

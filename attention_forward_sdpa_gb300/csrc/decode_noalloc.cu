@@ -17,10 +17,10 @@
 // (with that device current) and caches it.  That first call may load the
 // module, so make it before any stream capture.
 //
-// Every call on a device shares the one array and overwrites it completely
-// for the rows it uses (each split writes its partial o, m and l before the
-// combine reads them), so nothing has to start at zero and nothing of a
-// previous call is read.  Calls that can overlap on the device -- different
+// Every call on a device shares the one array.  Each call first zeroes the
+// work counter at the end of its part of the array (the only value that must
+// start at zero) and then overwrites every partial o, m and l before the
+// combine reads it, so nothing of a previous call is read.  Calls that can overlap on the device -- different
 // streams without ordering between them -- race on the array and must not be
 // issued.
 
@@ -99,7 +99,7 @@ extern "C" attn_status_t attn_fwd_decode_noalloc(
   if (major != 10 || minor != 3) return ATTN_ERR_UNSUPPORTED;
 
   void* scratch = nullptr;
-  if (need > 0 && scratch_address(&scratch) != cudaSuccess) return ATTN_ERR_CUDA;
+  if (scratch_address(&scratch) != cudaSuccess) return ATTN_ERR_CUDA;
 
   attn::DecodeParams p;
   std::memset(&p, 0, sizeof(p));
@@ -111,11 +111,6 @@ extern "C" attn_status_t attn_fwd_decode_noalloc(
   p.status = status_dev;
   p.block_table = block_table;
   p.seq_lens = seq_lens;
-  if (need > 0) {
-    const size_t rows = (size_t)num_seqs * num_q_heads * num_splits;
-    p.part_o = static_cast<float*>(scratch);
-    p.part_ml = p.part_o + rows * (size_t)head_size;
-  }
   p.bt_stride = block_table_stride;
   p.num_seqs = num_seqs;
   p.max_seqlen_k = max_seqlen_k;
@@ -126,7 +121,6 @@ extern "C" attn_status_t attn_fwd_decode_noalloc(
   p.num_splits = num_splits;
   p.rounding = (int32_t)rounding;
   p.scale_log2 = scale * 1.4426950408889634f;
-  cudaError_t e = attn::launch_decode(p, head_size, dtype == ATTN_BF16, num_q_heads / num_kv_heads,
-                                      static_cast<cudaStream_t>(stream));
-  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+  return (attn_status_t)attn::decode_prepare_and_launch(p, head_size, dtype == ATTN_BF16, scratch,
+                                                        static_cast<cudaStream_t>(stream));
 }

@@ -318,6 +318,13 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(const __grid_consta
   if (lane == 0 && p.lse) p.lse[row] = L > 0.f ? M * kLn2 + logf(L) : -INFINITY;
 }
 
+template <int D, bool BF16>
+cudaError_t launch_combine_t(const DecodeParams& p, cudaStream_t stream) {
+  const int64_t rows = (int64_t)p.num_seqs * p.num_q_heads;
+  decode_combine_kernel<D, BF16><<<(unsigned)((rows + 3) / 4), 128, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
 template <int D, bool BF16, int GH>
 cudaError_t launch_decode_t(const DecodeParams& p, cudaStream_t stream) {
   const int G = p.num_q_heads / p.num_kv_heads;
@@ -325,9 +332,7 @@ cudaError_t launch_decode_t(const DecodeParams& p, cudaStream_t stream) {
   decode_split_kernel<D, BF16, GH><<<grid, kDecWarps * 32, 0, stream>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || p.num_splits == 1) return e;
-  const int64_t rows = (int64_t)p.num_seqs * p.num_q_heads;
-  decode_combine_kernel<D, BF16><<<(unsigned)((rows + 3) / 4), 128, 0, stream>>>(p);
-  return cudaGetLastError();
+  return launch_combine_t<D, BF16>(p, stream);
 }
 
 template <int D, bool BF16>
@@ -363,6 +368,13 @@ cudaError_t launch_decode(const DecodeParams& p, int head_size, bool bf16, int g
   const int gh = heads_per_cta(group);
   if (head_size == 128) return bf16 ? launch_decode_d<128, true>(p, gh, stream) : launch_decode_d<128, false>(p, gh, stream);
   if (head_size == 64) return bf16 ? launch_decode_d<64, true>(p, gh, stream) : launch_decode_d<64, false>(p, gh, stream);
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_decode_combine(const DecodeParams& p, int head_size, bool bf16,
+                                  cudaStream_t stream) {
+  if (head_size == 128) return bf16 ? launch_combine_t<128, true>(p, stream) : launch_combine_t<128, false>(p, stream);
+  if (head_size == 64) return bf16 ? launch_combine_t<64, true>(p, stream) : launch_combine_t<64, false>(p, stream);
   return cudaErrorInvalidValue;
 }
 

@@ -103,7 +103,10 @@ attn_status_t attn_fwd_prefill(void* out, const void* q, const void* k_cache, co
 
 /*
  * attn_decode_workspace_size -- bytes of device workspace attn_fwd_decode
- * needs for these sizes (0 when num_splits == 1).  Pure host arithmetic.
+ * needs for these sizes: the split partials (num_seqs * num_q_heads *
+ * num_splits * (head_size + 2) fp32 values when num_splits > 1) plus 256
+ * bytes for the work counter of the persistent decode kernel.  Pure host
+ * arithmetic; 0 only for an empty problem.
  */
 size_t attn_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t head_size,
                                   int32_t num_splits);
@@ -126,9 +129,10 @@ size_t attn_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t
  *   num_splits   1 .. 64.
  *   lse_out      optional [num_seqs, num_q_heads] fp32, or NULL.
  *   workspace    device memory of at least attn_decode_workspace_size(...)
- *                bytes, 16-byte aligned (may be NULL when num_splits == 1);
- *                owned by the caller, overwritten by the call, and must not
- *                be shared by calls that overlap on the device.
+ *                bytes, 16-byte aligned; owned by the caller, any initial
+ *                contents (the call zeroes what must start at zero with an
+ *                asynchronous memset on `stream`), overwritten by the call,
+ *                and not to be shared by calls that overlap on the device.
  */
 attn_status_t attn_fwd_decode(void* out, const void* q, const void* k_cache, const void* v_cache,
                               const int32_t* block_table, int32_t block_table_stride,

@@ -62,8 +62,8 @@ def test_status_strings_and_version(lib):
 
 
 def test_workspace_size_is_arithmetic(lib):
-    assert lib.attn_decode_workspace_size(64, 32, 128, 8) == 64 * 32 * 8 * (128 + 2) * 4
-    assert lib.attn_decode_workspace_size(64, 32, 128, 1) == 0
+    assert lib.attn_decode_workspace_size(64, 32, 128, 8) == 64 * 32 * 8 * (128 + 2) * 4 + 256
+    assert lib.attn_decode_workspace_size(64, 32, 128, 1) == 256
     assert lib.attn_decode_workspace_size(0, 32, 128, 8) == 0
 
 
@@ -112,7 +112,7 @@ def test_prefill_empty_problem_is_a_no_op(lib):
 def decode_args(**over):
     a = dict(out=FAKE, q=FAKE, k=FAKE, v=FAKE, bt=FAKE, bt_stride=512, sl=FAKE, num_seqs=64,
              max_k=8192, hq=32, hkv=8, d=128, bs=16, nb=100000, scale=0.088, splits=8, dtype=1,
-             rounding=0, lse=None, ws=FAKE, ws_bytes=64 * 32 * 8 * 130 * 4, status=None,
+             rounding=0, lse=None, ws=FAKE, ws_bytes=64 * 32 * 8 * 130 * 4 + 256, status=None,
              stream=None)
     a.update(over)
     return [a[k] for k in ("out", "q", "k", "v", "bt", "bt_stride", "sl", "num_seqs", "max_k",

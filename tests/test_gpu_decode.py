@@ -32,7 +32,8 @@ def test_workload_decode_full():
     check(attn_inputs.workload("decode_bf16_b64_paged16"), splits=8)
 
 
-@pytest.mark.parametrize("hq,hkv", [(8, 8), (8, 4), (8, 2), (16, 2), (24, 2), (12, 4)])
+@pytest.mark.parametrize("hq,hkv", [(8, 8), (8, 4), (8, 2), (16, 2), (24, 2), (12, 4), (16, 1),
+                                     (32, 1), (40, 2)])
 def test_head_groups(hq, hkv):
     prob = attn_inputs.paged_problem(seed=31, q_lens=[1] * 5, kv_lens=[1, 16, 17, 300, 2049],
                                      num_q_heads=hq, num_kv_heads=hkv, head_size=128,
@@ -41,11 +42,37 @@ def test_head_groups(hq, hkv):
 
 
 @pytest.mark.parametrize("splits", [1, 2, 3, 8, 64])
-def test_split_counts(splits):
+@pytest.mark.parametrize("bs", [16, 32, 256])
+def test_split_counts(splits, bs):
     prob = attn_inputs.paged_problem(seed=32, q_lens=[1] * 4, kv_lens=[5, 64, 1000, 4097],
-                                     num_q_heads=8, num_kv_heads=2, head_size=128, block_size=32,
+                                     num_q_heads=8, num_kv_heads=2, head_size=128, block_size=bs,
                                      causal=False)
     check(prob, splits=splits)
+
+
+@pytest.mark.parametrize("splits", [1, 8])
+def test_fp16_d128(splits):
+    prob = attn_inputs.paged_problem(seed=38, q_lens=[1] * 3, kv_lens=[130, 9, 2500],
+                                     num_q_heads=16, num_kv_heads=4, head_size=128, block_size=16,
+                                     dtype=torch.float16, causal=False, sigma=2.0)
+    check(prob, splits=splits)
+
+
+def test_fp32_output_and_rounding_modes():
+    prob = attn_inputs.paged_problem(seed=39, q_lens=[1] * 6, kv_lens=[100, 2000, 33, 700, 1, 4000],
+                                     num_q_heads=8, num_kv_heads=2, head_size=128, block_size=16,
+                                     causal=False)
+    from oracle import oracle
+    t = to_dev(prob)
+    for splits in (1, 8):
+        x = gpu_decode(prob, t, splits=splits, rounding=3)
+        torch.cuda.synchronize()
+        xf = x.cpu().numpy().astype(np.float32)
+        for mode in (0, 1, 2):
+            r = gpu_decode(prob, t, splits=splits, rounding=mode)
+            torch.cuda.synchronize()
+            got = r.cpu().view(torch.int16).numpy().view(np.uint16)
+            assert np.array_equal(got, oracle.round_f32(xf, oracle.BF16, mode)), (splits, mode)
 
 
 def test_fp16_d64():
