@@ -34,6 +34,7 @@ constexpr int kBM = 128;        // query rows per tile
 constexpr int kBN = 128;        // keys per KV tile
 constexpr int kThreads = 384;   // 12 warps
 constexpr float kLn2 = 0.693147180559945309f;
+constexpr float kRescaleSlack = 8.f;  // log2 units: p stays <= 256
 
 template <int D>
 struct PrefillLayout {
@@ -340,38 +341,52 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
           for (int e = 0; e < 32; ++e)
             if (32 * c + e >= cl) s[c][e] = 0xFF800000u;  // -inf
       }
-      float mx = -INFINITY;
+      // row max over the tile's 128 scores (three-input max: 1 + 63 steps + 1)
+      float mx = __uint_as_float(s[0][0]);
 #pragma unroll
-      for (int c = 0; c < 4; ++c)
-#pragma unroll
-        for (int e = 0; e < 32; ++e) mx = fmaxf(mx, __uint_as_float(s[c][e]));
-      const float m_new = fmaxf(m, mx * sl2);
+      for (int i = 1; i + 1 < 128; i += 2)
+        mx = fmax3(mx, __uint_as_float(s[i >> 5][i & 31]), __uint_as_float(s[(i + 1) >> 5][(i + 1) & 31]));
+      mx = fmaxf(mx, __uint_as_float(s[3][31]));
+      // The running max is only raised when the tile's max exceeds it by
+      // more than kRescaleSlack (log2 units).  Any reference value works for
+      // the recurrence as long as o and l use the same one, so this is exact;
+      // it keeps p <= 2^kRescaleSlack and makes the O rescale rare.
+      const float mxs = mx * sl2;
+      const float m_new = (mxs > m + kRescaleSlack) ? mxs : m;
       const float m_use = m_new == -INFINITY ? 0.f : m_new;
       const float alpha = fast_exp2(m - m_use);
-      float rs = 0.f;
+      const float2 sc2 = make_float2(sl2, sl2);
+      const float2 nm2 = make_float2(-m_use, -m_use);
+      float2 rs2 = make_float2(0.f, 0.f);
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
-          const float p0 = fast_exp2(fmaf(__uint_as_float(s[c][2 * e]), sl2, -m_use));
-          const float p1 = fast_exp2(fmaf(__uint_as_float(s[c][2 * e + 1]), sl2, -m_use));
-          rs += p0 + p1;
-          pk[e] = BF16 ? pack_bf16x2_rn(p0, p1) : pack_f16x2_rn(p0, p1);
+          const float2 x = ffma2(make_float2(__uint_as_float(s[c][2 * e]), __uint_as_float(s[c][2 * e + 1])),
+                                 sc2, nm2);
+          const float2 pp = make_float2(fast_exp2(x.x), fast_exp2(x.y));
+          rs2 = fadd2(rs2, pp);
+          pk[e] = BF16 ? pack_bf16x2_rn(pp.x, pp.y) : pack_f16x2_rn(pp.x, pp.y);
         }
         tmem_st16(tS + 16 * c, pk);
       }
-      l = l * alpha + rs;
+      l = l * alpha + (rs2.x + rs2.y);
       if (j > 0 && __any_sync(0xFFFFFFFFu, alpha != 1.f)) {
         // O_t is final for tile j-1 here: S_t(j) was issued after PV_t(j-1)
         // and its commit covers every earlier MMA.
+        const float2 a2 = make_float2(alpha, alpha);
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t o[32];
           tmem_ld32(tO + 32 * c, o);
           tmem_ld_wait(o);
 #pragma unroll
-          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+          for (int e = 0; e < 16; ++e) {
+            const float2 v = fmul2(make_float2(__uint_as_float(o[2 * e]), __uint_as_float(o[2 * e + 1])), a2);
+            o[2 * e] = __float_as_uint(v.x);
+            o[2 * e + 1] = __float_as_uint(v.y);
+          }
           tmem_st32(tO + 32 * c, o);
         }
       }

@@ -59,8 +59,8 @@ CSRC = os.path.join(ROOT, "attention_forward_sdpa_gb300", "csrc")
 # workload, valid only while the kernel source has the recorded sha256 prefix
 # (the ncu summaries under profiles/ record each capture).
 MEASURED_TRAFFIC = {
-    "prefill": ("prefill_tcgen05.cu", "3051df3ce90d87f5", 25.234944e6 + 1.024e3),
-    "decode": ("decode_splitkv.cu", "8b599f75bfa6c318", 1.129085e9 + 11.666944e6),
+    "prefill": ("prefill_tcgen05.cu", "76bc50f1e2d6f0fb", 25.23264e6 + 1.536e3),
+    "decode": ("decode_tcgen05.cu", "41ba06cc4fe2f02a", 1.130848e9 + 11.470848e6),
 }
 
 
@@ -268,7 +268,7 @@ def run_ours(args, rank, world, dev):
               "traffic": measured_traffic("prefill"),
               "peak_source": f"{peak_src} bf16 burst", "avg_launch_us": p_avg_s * 1e6,
               "algorithmic_per_launch": flops}
-    roof_d = {"kernel": "decode_split_kernel<128,bf16,4> + decode_combine_kernel", "bound": "hbm",
+    roof_d = {"kernel": "decode_tc_kernel<bf16,4> + decode_combine_kernel", "bound": "hbm",
               "achieved": dbytes / d_avg_s / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s",
               "frac": dbytes / d_avg_s / 1e9 / peaks["hbm_gbs"],
               "traffic": measured_traffic("decode"),
