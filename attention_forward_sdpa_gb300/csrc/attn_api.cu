@@ -87,6 +87,7 @@ int decode_prepare_and_launch(DecodeParams& p, int head_size, bool bf16, void* w
                               cudaStream_t stream) {
   const size_t rows = (size_t)p.num_seqs * (size_t)p.num_q_heads * (size_t)p.num_splits;
   float* ws = static_cast<float*>(workspace);
+  const size_t counter_bytes = 256;
   if (p.num_splits > 1) {
     p.part_o = ws;
     p.part_ml = ws + rows * (size_t)head_size;
@@ -97,18 +98,28 @@ int decode_prepare_and_launch(DecodeParams& p, int head_size, bool bf16, void* w
     p.counter = reinterpret_cast<int32_t*>(ws);
   }
   const int G = p.num_q_heads / p.num_kv_heads;
-  const bool tc_path = head_size == 128 && (G <= 16 || G % 16 == 0);
+  const bool pow2 = (G & (G - 1)) == 0;
+  const bool tc_path = head_size == 128 && ((G <= 16 && pow2) || G % 16 == 0);
   if (!tc_path) {
     cudaError_t e = launch_decode(p, head_size, bf16, G, stream);
     return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
   }
   p.heads_per_item = G <= 16 ? G : 16;
+  // KV heads per item: as many as divide Hkv, fit 16 query-head columns, <= 4
+  p.kv_per_item = 1;
+  for (int f = 4; f > 1; f >>= 1)
+    if (p.num_kv_heads % f == 0 && f * p.heads_per_item <= 16) {
+      p.kv_per_item = f;
+      break;
+    }
   p.q_box_rows = p.num_q_heads < 16 ? p.num_q_heads : 16;
-  const int64_t n_items =
-      (int64_t)p.num_seqs * (p.num_q_heads / p.heads_per_item) * (int64_t)p.num_splits;
+  const int64_t n_items = (int64_t)p.num_seqs * (p.num_kv_heads / p.kv_per_item) *
+                          (G / p.heads_per_item) * (int64_t)p.num_splits;
   if (n_items > 2147483647) return ATTN_ERR_UNSUPPORTED;
   p.n_items = (int32_t)n_items;
   const cuuint64_t d = (cuuint64_t)head_size;
+  const cuuint64_t slot_stride = d * 2 * (cuuint64_t)p.num_kv_heads;
+  const cuuint64_t block_stride = slot_stride * (cuuint64_t)p.block_size;
   {
     const cuuint64_t dims[3] = {d, (cuuint64_t)p.num_q_heads, (cuuint64_t)p.num_seqs};
     const cuuint64_t strides[2] = {d * 2, d * 2 * (cuuint64_t)p.num_q_heads};
@@ -117,19 +128,29 @@ int decode_prepare_and_launch(DecodeParams& p, int head_size, bool bf16, void* w
       return ATTN_ERR_CUDA;
   }
   {
-    const cuuint64_t dims[4] = {d, (cuuint64_t)p.num_kv_heads, (cuuint64_t)p.block_size,
+    // K as (channel, slot, head, page): a box of 16 slots x F heads lands as
+    // 16F consecutive rows of 64 channels
+    const cuuint64_t dims[4] = {d, (cuuint64_t)p.block_size, (cuuint64_t)p.num_kv_heads,
                                 (cuuint64_t)p.num_blocks};
-    const cuuint64_t strides[3] = {d * 2, d * 2 * (cuuint64_t)p.num_kv_heads,
-                                   d * 2 * (cuuint64_t)p.num_kv_heads * (cuuint64_t)p.block_size};
-    const cuuint32_t box[4] = {64, 1, 16, 1};
-    if (!encode_tiled(&p.tm_k, bf16, 4, dims, strides, box, p.k_cache, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_tiled(&p.tm_v, bf16, 4, dims, strides, box, p.v_cache, CU_TENSOR_MAP_SWIZZLE_128B))
+    const cuuint64_t strides[3] = {slot_stride, d * 2, block_stride};
+    const cuuint32_t box[4] = {64, 16, (cuuint32_t)p.kv_per_item, 1};
+    if (!encode_tiled(&p.tm_k, bf16, 4, dims, strides, box, p.k_cache, CU_TENSOR_MAP_SWIZZLE_128B))
+      return ATTN_ERR_CUDA;
+  }
+  {
+    // V as (channel in half, slot, channel half, head, page): one box brings
+    // both channel halves of 16 slots x F heads
+    const cuuint64_t dims[5] = {64, (cuuint64_t)p.block_size, 2, (cuuint64_t)p.num_kv_heads,
+                                (cuuint64_t)p.num_blocks};
+    const cuuint64_t strides[4] = {slot_stride, 128, d * 2, block_stride};
+    const cuuint32_t box[5] = {64, 16, 2, (cuuint32_t)p.kv_per_item, 1};
+    if (!encode_tiled(&p.tm_v, bf16, 5, dims, strides, box, p.v_cache, CU_TENSOR_MAP_SWIZZLE_128B))
       return ATTN_ERR_CUDA;
   }
   const int sms = device_sm_count();
   if (sms <= 0) return ATTN_ERR_CUDA;
   const int grid = (int)(n_items < sms ? n_items : sms);
-  if (cudaMemsetAsync(p.counter, 0, sizeof(int32_t), stream) != cudaSuccess) return ATTN_ERR_CUDA;
+  if (cudaMemsetAsync(p.counter, 0, counter_bytes, stream) != cudaSuccess) return ATTN_ERR_CUDA;
   cudaError_t e = launch_decode_tc(p, bf16, grid, stream);
   if (e == cudaSuccess && p.num_splits > 1) e = launch_decode_combine(p, head_size, bf16, stream);
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;

@@ -38,11 +38,12 @@ struct PrefillParams {
 
 struct DecodeParams {
   CUtensorMap tm_q;     // Q [num_seqs, Hq, d]: dims (d, Hq, num_seqs), box (64, min(16, Hq), 1)
-  CUtensorMap tm_k;     // K cache: dims (d, Hkv, bs, num_blocks), box (64, 1, 16, 1)
-  CUtensorMap tm_v;     // V cache: same
+  CUtensorMap tm_k;     // K cache: dims (d, bs, Hkv, num_blocks), box (64, 16, F, 1)
+  CUtensorMap tm_v;     // V cache: dims (64, bs, 2, Hkv, num_blocks), box (64, 16, 2, F, 1)
   int32_t* counter;     // work counter of the persistent kernel (zeroed before the launch)
   int32_t n_items;      // num_seqs * (Hq / heads_per_item) * num_splits
-  int32_t heads_per_item;
+  int32_t heads_per_item;  // query heads per KV head in a work item
+  int32_t kv_per_item;     // KV heads per work item
   int32_t q_box_rows;
   const void* q;        // [num_seqs, Hq, d]
   const void* k_cache;  // [num_blocks, bs, Hkv, d]

@@ -2,27 +2,35 @@
 // math up", sec. 8) for head size 128 as a persistent, TMA-fed, tcgen05
 // kernel.  Decode is bound by HBM bandwidth (each K/V byte is read once and
 // used for 2 * G flops), so the design goal is a continuous stream of page
-// loads with almost no instructions per byte:
+// loads with as few instructions per byte as possible:
 //
-//   * work items are (sequence, group of query heads sharing a KV head,
-//     split); persistent CTAs (one per SM) claim them from an atomic counter,
-//     so items of different length balance dynamically and the load pipeline
-//     never drains between items;
-//   * warp 0 streams each item's Q rows and its pages as 16-row TMA boxes
-//     (128-byte swizzle) into a ring of 32 KB key tiles (K and V alternate);
-//     its lanes issue the boxes of a tile in parallel;
-//   * warp 1 issues S^T = K Q^T (M = 128 keys, N = 16 query heads, fp32 in
-//     TMEM) and O^T += V^T P^T (M = 128 channels, N = 16): with the keys on M
-//     one thread owns one key's scores;
-//   * warps 2-5 (one thread per key, then per channel) take each tile's
-//     scores from TMEM, form the running max across the CTA, exp2, the
-//     running denominators, write P^T (16-bit) to shared memory, rescale O^T
-//     in TMEM when the max moved, and at the end of an item write the partial
-//     state (un-normalised o, max in log2 units, denominator) -- or, with one
-//     split, the final rounded output.
-// S^T is double-buffered so the next tile's product overlaps this tile's
-// softmax.  Every wait is bounded (see sm103_ptx.cuh); the CTA-wide exchange
-// of the softmax warps also goes through an mbarrier so that it is bounded.
+//   * A work item is (sequence, F consecutive KV heads, split) -- F KV heads
+//     and all their query heads (F * G <= 16) at once, so that one TMA box
+//     brings the same 16 page rows of F heads: with the cache viewed as
+//     (channel, slot, head, page) a box of 64 channels x 16 slots x F heads
+//     lands in shared memory as 16F consecutive 128-byte rows, and a 5-D view
+//     (channel, slot, channel half, head, page) fetches both channel halves
+//     of V in one instruction.  A 128-row key tile costs 3 * 8 / F TMA
+//     instructions (6 for F = 4) instead of 32 with one head per item.
+//   * Persistent CTAs (one per SM) claim items from an atomic counter in
+//     longest-sequence-first order (each CTA ranks the sequence lengths it
+//     caches in shared memory), so items balance dynamically.
+//   * Warp 0 streams Q rows and page boxes into a ring of 32 KB tiles (K and
+//     V alternate); its lanes hold the page ids of 64 boxes at a time and
+//     issue the boxes in parallel.
+//   * Warp 1 issues S^T = K Q^T (M = 128 tile rows, N = 16 query heads, fp32
+//     in TMEM) and O^T += V^T P^T (M = 128 channels, N = 16).  P^T is block
+//     diagonal (a row of KV head h only feeds the columns of h's query
+//     heads); the off-diagonal zeros are written once.
+//   * Warps 2-5 (one thread per tile row -- (box, KV head, key) -- then per
+//     channel) take each tile's scores from TMEM, form the per-column running
+//     max across the CTA (lazy: raised only when the tile's max exceeds it by
+//     more than 8 in log2 units, which is exact and makes O rescales rare),
+//     exp2, the running denominators, write P^T, rescale O^T when needed, and
+//     at the end of an item write the partial state (un-normalised o, max in
+//     log2 units, denominator) -- or, with one split, the rounded output.
+// Every wait is bounded (see sm103_ptx.cuh); the CTA-wide exchange of the
+// softmax warps also goes through an mbarrier so that it is bounded.
 
 #include "attn_internal.h"
 #include "round16.cuh"
@@ -32,31 +40,38 @@ namespace attn {
 namespace {
 
 constexpr int kD = 128;                 // head size handled here
-constexpr int kTK = 128;                // keys per tile
+constexpr int kRows = 128;              // tile rows: 16-key boxes x F heads x 16 keys
 constexpr int kThreads = 192;
 constexpr int kSlots = 6;               // K/V ring slots of one tile each
 constexpr int kItemRing = 4;
-constexpr int kTileBytes = kTK * kD * 2;        // 32 KB
-constexpr int kHalfBytes = kTK * 128;           // 128 keys x 64 channels
+constexpr int kTileBytes = kRows * kD * 2;      // 32 KB
+constexpr int kHalfBytes = kRows * 128;         // K: 128 rows x 64 channels
 constexpr int kQBytes = 2 * 16 * 128;           // two channel halves of [16 heads][64]
-constexpr int kPBytes = 2 * 16 * 128;           // two key halves of [16 heads][64 keys]
+constexpr int kPBytes = 2 * 16 * 128;           // two row halves of [16 heads][64 rows]
+constexpr int kSeqCache = 2048;                 // cached sequence lengths
+constexpr int kSortMax = 128;                   // longest-first order up to this many sequences
 constexpr float kLn2 = 0.693147180559945309f;
+constexpr float kRescaleSlack = 8.f;            // log2 units
 
 struct ItemEntry {
   int b;       // sequence, or -1 at the end of the work
-  int hg;      // head group: query heads [hg * heads_per_item, ...)
+  int kvh0;    // first KV head of the item
+  int q0;      // first query head of the item (column 0)
   int split;
   int k0, k1;  // key range
-  int pad[3];
+  int pad[2];
 };
 
 constexpr int kRingOff = 0;
 constexpr int kQOff = kRingOff + kSlots * kTileBytes;
 constexpr int kPOff = kQOff + 2 * kQBytes;
-constexpr int kRedOff = kPOff + 2 * kPBytes;            // float [2][4][16]
-constexpr int kLRedOff = kRedOff + 2 * 4 * 16 * 4;      // float [2][4][16]
-constexpr int kItemOff = kLRedOff + 2 * 4 * 16 * 4;     // ItemEntry [kItemRing]
-constexpr int kBarOff = kItemOff + kItemRing * (int)sizeof(ItemEntry);
+constexpr int kRedOff = kPOff + 2 * kPBytes;            // float [2][8 groups][16]
+constexpr int kLRedOff = kRedOff + 2 * 8 * 16 * 4;      // float [2][8 groups][16]
+constexpr int kItemOff = kLRedOff + 2 * 8 * 16 * 4;     // ItemEntry [kItemRing]
+constexpr int kSeqOff = kItemOff + kItemRing * (int)sizeof(ItemEntry);
+constexpr int kOrderOff = kSeqOff + kSeqCache * 4;
+constexpr int kFlagOff = kOrderOff + kSortMax * 4;          // int [3]
+constexpr int kBarOff = kFlagOff + 16;
 // barriers: kv_full[kSlots] kv_empty[kSlots] q_full[2] q_empty[2] s_full[2]
 //           p_full[2] pv_done item_full[R] item_empty[R] mma_done red
 constexpr int kNumBars = 2 * kSlots + 2 + 2 + 2 + 2 + 1 + 2 * kItemRing + 1 + 1;
@@ -83,15 +98,15 @@ __device__ __forceinline__ void split_keys(int Sk, int splits, int s, int& k0, i
   k1 = min(Sk, k0 + per);
 }
 
-// Byte offset of the 16-bit P^T element (head h, key k) in the K-major,
-// 128-byte-swizzled B operand: two key halves of [16 heads][64 keys].
-__device__ __forceinline__ uint32_t p_offset(int h, int k) {
-  const int half = k >> 6, c = k & 63;
-  const int chunk = (c >> 3) ^ (h & 7);
-  return (uint32_t)(half * 2048 + h * 128 + chunk * 16 + (c & 7) * 2);
+// Byte offset of the 16-bit P^T element (column q, tile row r) in the
+// K-major, 128-byte-swizzled B operand: two row halves of [16 columns][64].
+__device__ __forceinline__ uint32_t p_offset(int q, int r) {
+  const int half = r >> 6, c = r & 63;
+  const int chunk = (c >> 3) ^ (q & 7);
+  return (uint32_t)(half * 2048 + q * 128 + chunk * 16 + (c & 7) * 2);
 }
 
-template <bool BF16, int NH>
+template <bool BF16, int GH>
 __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_constant__ DecodeParams p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -103,6 +118,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
   float* red = reinterpret_cast<float*>(smem + kRedOff);
   float* lred = reinterpret_cast<float*>(smem + kLRedOff);
   ItemEntry* items = reinterpret_cast<ItemEntry*>(smem + kItemOff);
+  int* seq_cache = reinterpret_cast<int*>(smem + kSeqOff);
+  int* order = reinterpret_cast<int*>(smem + kOrderOff);
   const uint32_t bars = base + kBarOff;
   const uint32_t bar_kv_full = bars;
   const uint32_t bar_kv_empty = bars + 8u * kSlots;
@@ -120,9 +137,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int GH = p.heads_per_item;
-  const int hgroups = p.num_q_heads / GH;
+  const int F = p.kv_per_item;              // KV heads per item (GH * F <= 16)
+  const int KT = kRows / F;                 // keys per tile
+  const int BPT = KT / 16;                  // 16-key boxes per tile
   const int G = p.num_q_heads / p.num_kv_heads;
+  const int subs = G / GH;                  // query-head groups per KV head (1 unless G > 16)
+  const int groups = (p.num_kv_heads / F) * subs;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kSlots; ++s) {
@@ -142,9 +162,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
     }
     mbar_init(bar_mma_done, 1);
     mbar_init(bar_red, 128);
+    for (int i = 0; i < 3; ++i) reinterpret_cast<volatile int*>(smem + kFlagOff)[i] = 0;
     *abort_flag = 0;
     fence_mbar_init();
   }
+  // P^T is block diagonal: zero both buffers once; each softmax thread later
+  // writes only its own (row, column) entries
+  for (int i = threadIdx.x; i < 2 * kPBytes / 16; i += kThreads)
+    reinterpret_cast<uint4*>(smem + kPOff)[i] = make_uint4(0u, 0u, 0u, 0u);
+  fence_proxy_async_smem();
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&p.tm_q);
     tma_prefetch_desc(&p.tm_k);
@@ -166,18 +192,56 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
     uint32_t last_fill[kSlots];
 #pragma unroll
     for (int s = 0; s < kSlots; ++s) last_fill[s] = 0;
+    const bool cached = p.num_seqs <= kSeqCache;
+    if (cached)
+      for (int i = lane; i < p.num_seqs; i += 32) seq_cache[i] = p.seq_lens[i];
+    __syncwarp();
+    // longest sequences first (ties by index), so that the dynamic queue
+    // ends with short items
+    const bool sorted = cached && p.num_seqs <= kSortMax;
+    if (sorted) {
+      for (int b = lane; b < p.num_seqs; b += 32) {
+        const int lb = seq_cache[b];
+        int rank = 0;
+        for (int c = 0; c < p.num_seqs; ++c) {
+          const int lc = seq_cache[c];
+          rank += (lc > lb || (lc == lb && c < b)) ? 1 : 0;
+        }
+        order[rank] = b;
+      }
+    }
+    __syncwarp();
+    // page ids of 64 boxes (1024 keys) at a time, two per lane: box q is held
+    // by lane q % 32 in register q / 32, and that lane issues the box
+    auto load_ids = [&](const int32_t* bt, int k0, int n_boxes, int cb, int (&pg)[2], int (&rw)[2]) {
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        pg[h] = 0;
+        rw[h] = 0;
+        const int q = cb + 32 * h + lane;
+        if (q < n_boxes) {
+          const int key = k0 + 16 * q;
+          pg[h] = bt[key / bs];
+          rw[h] = key % bs;
+          if (pg[h] < 0 || pg[h] >= p.num_blocks) report_status(p.status, kStatusBadBlockTable);
+        }
+      }
+    };
     for (;;) {
       int item = 0;
       if (lane == 0) item = atomicAdd(p.counter, 1);
       item = __shfl_sync(0xFFFFFFFFu, item, 0);
       const bool end = item >= p.n_items;
-      int b = -1, hg = 0, split = 0, k0 = 0, k1 = 0;
+      int b = -1, kvh0 = 0, q0 = 0, split = 0, k0 = 0, k1 = 0;
       if (!end) {
         split = item % p.num_splits;
         const int rest = item / p.num_splits;
-        hg = rest % hgroups;
-        b = rest / hgroups;
-        int Sk = p.seq_lens[b];
+        const int grp = rest % groups;
+        const int rank = rest / groups;
+        b = sorted ? order[rank] : rank;
+        kvh0 = (grp / subs) * F;
+        q0 = kvh0 * G + (grp % subs) * GH;
+        int Sk = cached ? seq_cache[b] : p.seq_lens[b];
         if (Sk < 0 || Sk > p.max_seqlen_k) {
           if (lane == 0) report_status(p.status, kStatusBadArg);
           Sk = 0;
@@ -190,57 +254,65 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
         break;
       if (lane == 0) {
         ItemEntry e;
-        e.b = b; e.hg = hg; e.split = split; e.k0 = k0; e.k1 = k1;
-        e.pad[0] = e.pad[1] = e.pad[2] = 0;
+        e.b = b; e.kvh0 = kvh0; e.q0 = q0; e.split = split; e.k0 = k0; e.k1 = k1;
+        e.pad[0] = e.pad[1] = 0;
         items[rs] = e;
         mbar_arrive(bar_item_full + 8u * rs);
       }
       __syncwarp();
       ++seen;
       if (end) break;
-      const int n_tiles = (k1 - k0 + kTK - 1) / kTK;
+      const int n_tiles = (k1 - k0 + KT - 1) / KT;
       if (n_tiles == 0) continue;
-      const int kvh = (hg * GH) / G;
-      // Q rows of the head group
+      // Q rows of the item's query heads
       const uint32_t qs = q_loads & 1u;
       if (q_loads >= 2 && !mbar_wait(bar_q_empty + 8u * qs, ((q_loads >> 1) - 1) & 1, abort_flag))
         break;
       if (lane == 0) {
         mbar_arrive_expect_tx(bar_q_full + 8u * qs, (uint32_t)(2 * p.q_box_rows * 128));
         for (int h = 0; h < 2; ++h)
-          tma_load_3d(sQ + qs * kQBytes + h * 2048, &p.tm_q, bar_q_full + 8u * qs, h * 64, hg * GH, b);
+          tma_load_3d(sQ + qs * kQBytes + h * 2048, &p.tm_q, bar_q_full + 8u * qs, h * 64, q0, b);
       }
       ++q_loads;
       const int32_t* bt = p.block_table + (int64_t)b * p.bt_stride;
+      const int n_boxes = (k1 - k0 + 15) / 16;
       bool ok = true;
-      for (int t = 0; t < n_tiles && ok; ++t) {
-        const int tk0 = k0 + t * kTK;
-        const int nbox = (min(kTK, k1 - tk0) + 15) / 16;
-        int page = 0, row = 0;
-        if (lane < nbox) {
-          const int key = tk0 + 16 * lane;
-          page = bt[key / bs];
-          row = key % bs;
-          if (page < 0 || page >= p.num_blocks) report_status(p.status, kStatusBadBlockTable);
-        }
-        for (int kind = 0; kind < 2; ++kind) {
-          const uint32_t s = fills % kSlots;
-          if (fills >= kSlots &&
-              !mbar_wait(bar_kv_empty + 8u * s, ((fills / kSlots) - 1) & 1, abort_flag)) {
-            ok = false;
-            break;
+      for (int cb = 0; cb < n_boxes && ok; cb += 64) {
+        int pg[2], rw[2];
+        load_ids(bt, k0, n_boxes, cb, pg, rw);
+        const int chunk_boxes = min(64, n_boxes - cb);
+        for (int rb = 0; rb < chunk_boxes && ok; rb += BPT) {
+          const int nbox = min(BPT, chunk_boxes - rb);
+          const int set = rb >> 5;            // register holding this tile's ids
+          const int j = lane - (rb & 31);     // this lane's box within the tile
+          const bool mine = j >= 0 && j < nbox;
+          const int page = set ? pg[1] : pg[0];
+          const int row = set ? rw[1] : rw[0];
+          for (int kind = 0; kind < 2; ++kind) {
+            const uint32_t s = fills % kSlots;
+            if (fills >= kSlots &&
+                !mbar_wait(bar_kv_empty + 8u * s, ((fills / kSlots) - 1) & 1, abort_flag)) {
+              ok = false;
+              break;
+            }
+            const uint32_t bar = bar_kv_full + 8u * s;
+            if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)(nbox * F * 4096));
+            __syncwarp();
+            if (mine) {
+              const uint32_t slot = sRing + s * kTileBytes;
+              if (kind == 0) {
+                // K: [channel half][tile row], box j -> rows [16 F j, 16 F (j + 1))
+                const uint32_t dst = slot + j * F * 16 * 128;
+                tma_load_4d(dst, &p.tm_k, bar, 0, row, kvh0, page);
+                tma_load_4d(dst + kHalfBytes, &p.tm_k, bar, 64, row, kvh0, page);
+              } else {
+                // V: [16-row group][channel half][16 rows], both halves at once
+                tma_load_5d(slot + j * F * 4096, &p.tm_v, bar, 0, row, 0, kvh0, page);
+              }
+            }
+            last_fill[s] = fills + 1;
+            ++fills;
           }
-          const uint32_t bar = bar_kv_full + 8u * s;
-          if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)(nbox * 2 * 2048));
-          __syncwarp();
-          if (lane < nbox) {
-            const CUtensorMap* tm = kind ? &p.tm_v : &p.tm_k;
-            const uint32_t dst = sRing + s * kTileBytes + lane * 16 * 128;
-            tma_load_4d(dst, tm, bar, 0, kvh, row, page);
-            tma_load_4d(dst + kHalfBytes, tm, bar, 64, kvh, row, page);
-          }
-          last_fill[s] = fills + 1;
-          ++fills;
         }
       }
       if (!ok) break;
@@ -270,8 +342,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
         const uint32_t a0 = sRing + sv * kTileBytes;
         const uint32_t b0 = sP + (pend_g & 1u) * kPBytes;
 #pragma unroll
-        for (int kk = 0; kk < kTK / 16; ++kk) {
-          umma_ss(tmem + kOCol, make_sdesc_sw128(a0 + kk * 16 * 128, kHalfBytes, 1024),
+        for (int kk = 0; kk < kRows / 16; ++kk) {
+          // A = V^T (MN-major): 16 rows per step, channel halves 2048 B apart
+          umma_ss(tmem + kOCol, make_sdesc_sw128(a0 + kk * 4096, 2048, 1024),
                   make_sdesc_sw128(b0 + (kk >> 2) * 2048 + (kk & 3) * 32, 16, 1024), idesc_pv,
                   (pend_first && kk == 0) ? 0u : 1u);
         }
@@ -289,7 +362,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
       if (leader) mbar_arrive(bar_item_empty + 8u * rs);
       ++seen;
       if (e.b < 0) break;
-      const int n_tiles = (e.k1 - e.k0 + kTK - 1) / kTK;
+      const int n_tiles = (e.k1 - e.k0 + KT - 1) / KT;
       if (n_tiles == 0) continue;
       const uint32_t qs = q_uses & 1u;
       if (!mbar_wait(bar_q_full + 8u * qs, (q_uses >> 1) & 1, abort_flag)) { ok = false; break; }
@@ -334,9 +407,16 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
     drain_wait(bar_mma_done, 0);
   } else {
     // ---------------------------------------------------------- softmax + epilogue
-    const int sw = warp - 2;                 // 0..3
     const int quarter = warp & 3;            // TMEM lane quarter of this warp
-    const int r = quarter * 32 + lane;       // key (for S^T) / channel (for O^T)
+    const int r = quarter * 32 + lane;       // tile row (S^T) / channel (O^T)
+    const int grp16 = r >> 4;                // (box, head) group of the row: box * F + head
+    const int hrow = grp16 % F;              // KV head of the row within the item
+    const int krow = (grp16 / F) * 16 + (r & 15);   // key of the row within the tile
+    const int c0 = hrow * GH;                // first column of the row's query heads
+    const int NC = F * GH;                   // columns in use
+    const int NG = kRows / 16;               // (box, head) groups per tile
+    constexpr int SW = GH == 16 ? 16 : 2 * GH;   // score columns loaded per warp
+    const int cwin = F >= 2 ? ((2 * quarter) % F) * GH : 0;
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     const float sl2 = p.scale_log2;
     const int Hq = p.num_q_heads;
@@ -356,47 +436,96 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
       if (lane == 0) mbar_arrive(bar_item_empty + 8u * rs);
       ++seen;
       if (e.b < 0) break;
-      const int n_tiles = (e.k1 - e.k0 + kTK - 1) / kTK;
-      float m[NH], lp[NH];
+      const int n_tiles = (e.k1 - e.k0 + KT - 1) / KT;
+      float mcol[16];   // running max of every column (kept identically by all threads)
 #pragma unroll
-      for (int h = 0; h < NH; ++h) { m[h] = -INFINITY; lp[h] = 0.f; }
+      for (int c = 0; c < 16; ++c) mcol[c] = -INFINITY;
+      // running max of the row's own columns (identical in every thread of
+      // the same KV head), partial denominators of this thread's keys
+      float m[GH], lp[GH];
+#pragma unroll
+      for (int j = 0; j < GH; ++j) {
+        m[j] = -INFINITY;
+        lp[j] = 0.f;
+      }
       for (int t = 0; t < n_tiles && ok; ++t) {
         if (!mbar_wait(bar_s_full + 8u * (g & 1u), (g >> 1) & 1, abort_flag)) { ok = false; break; }
         tc_fence_after();
-        uint32_t sv[NH];
-        tmem_ld_n<NH>(tmem + lane_off + s_col(g), sv);
-        tmem_ld_wait_n<NH>(sv);
-        const int key = e.k0 + t * kTK + r;
-        const bool valid = key < e.k1;
-        float x[NH];
+        // the warp's rows belong to one KV head (F = 1) or two adjacent ones:
+        // load their 2 * GH columns and keep this lane's half
+        uint32_t sv[SW];
+        tmem_ld_n<SW>(tmem + lane_off + s_col(g) + cwin, sv);
+        tmem_ld_wait_n<SW>(sv);
+        const bool valid = e.k0 + t * KT + krow < e.k1;
+        const bool upper = SW > GH && F >= 2 && lane >= 16;
+        float x[GH];
+        bool raise = false;
 #pragma unroll
-        for (int h = 0; h < NH; ++h) x[h] = valid ? __uint_as_float(sv[h]) * sl2 : -INFINITY;
-        // CTA-wide max per head
-        float* rb = red + (red_uses & 1u) * 64;
-#pragma unroll
-        for (int h = 0; h < NH; ++h) {
-          float v = x[h];
-#pragma unroll
-          for (int o = 16; o >= 1; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
-          if (lane == 0) rb[sw * 16 + h] = v;
+        for (int j = 0; j < GH; ++j) {
+          const float v = __uint_as_float(upper ? sv[(GH + j) % SW] : sv[j]);
+          x[j] = valid ? v * sl2 : -INFINITY;
+          raise |= x[j] > m[j] + kRescaleSlack;
         }
+        // Announce before the exchange whether any score of this tile exceeds
+        // its column's running max by more than the slack: only then does the
+        // max move (and O^T need a rescale).  Flags rotate over three words;
+        // the word for tile t + 1 is cleared here, before anyone can pass
+        // this tile's exchange and write it.
+        volatile int* flags = reinterpret_cast<volatile int*>(smem + kFlagOff);
+        const uint32_t fi = red_uses % 3u;
+        if (r == 0) flags[(fi + 1u) % 3u] = 0;
+        if (t == 0 || raise) flags[fi] = 1;
         if (!cta_sync()) { ok = false; break; }
-        float alpha[NH], mu[NH];
+        const bool heavy = flags[fi] != 0;
+        float alpha_own[GH];
+#pragma unroll
+        for (int j = 0; j < GH; ++j) alpha_own[j] = 1.f;
         bool rescale = false;
+        float alpha_all[16];
+        if (heavy) {
+          // the tile max of every column: 16-key maxima of each (box, head)
+          // group, then across boxes
+          float* rb = red + (red_uses & 1u) * 128;
 #pragma unroll
-        for (int h = 0; h < NH; ++h) {
-          const float tm = fmaxf(fmaxf(rb[h], rb[16 + h]), fmaxf(rb[32 + h], rb[48 + h]));
-          const float mn = fmaxf(m[h], tm);
-          mu[h] = mn == -INFINITY ? 0.f : mn;
-          alpha[h] = fast_exp2(m[h] - mu[h]);
-          rescale |= alpha[h] != 1.f;
-          m[h] = mn;
+          for (int j = 0; j < GH; ++j) {
+            float v = x[j];
+#pragma unroll
+            for (int o = 8; o >= 1; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+            if ((lane & 15) == 0) rb[grp16 * 16 + j] = v;
+          }
+          if (!cta_sync()) { ok = false; break; }
+#pragma unroll
+          for (int c = 0; c < 16; ++c) alpha_all[c] = 1.f;
+#pragma unroll
+          for (int c = 0; c < 16; ++c) {
+            if (c >= NC) break;
+            const int hh = c / GH, jj = c % GH;
+            float tm = -INFINITY;
+            for (int gg = hh; gg < NG; gg += F) tm = fmaxf(tm, rb[gg * 16 + jj]);
+            const float mo = mcol[c];
+            const float mn = (tm > mo + kRescaleSlack || mo == -INFINITY) ? fmaxf(tm, mo) : mo;
+            const float a = mo == -INFINITY ? 0.f : fast_exp2(mo - mn);
+            if (c / GH == hrow) {
+#pragma unroll
+              for (int j = 0; j < GH; ++j)
+                if (j == jj) {
+                  alpha_own[j] = a;
+                  m[j] = mn;
+                }
+            }
+#pragma unroll
+            for (int cc = 0; cc < 16; ++cc)
+              if (cc == c) alpha_all[cc] = a;
+            rescale |= a != 1.f;
+            mcol[c] = mn;
+          }
         }
-        float pr[NH];
+        float pr[GH];
 #pragma unroll
-        for (int h = 0; h < NH; ++h) {
-          pr[h] = fast_exp2(x[h] - mu[h]);
-          lp[h] = fmaf(lp[h], alpha[h], pr[h]);
+        for (int j = 0; j < GH; ++j) {
+          const float mu = m[j] == -INFINITY ? 0.f : m[j];
+          pr[j] = fast_exp2(x[j] - mu);
+          lp[j] = fmaf(lp[j], alpha_own[j], pr[j]);
         }
         // PV of the previous tile must be complete before O^T and the P^T
         // buffer of two tiles ago are touched
@@ -404,34 +533,34 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
           if (!mbar_wait(bar_pv_done, (g - 1) & 1, abort_flag)) { ok = false; break; }
           tc_fence_after();
         }
-        if (t > 0 && rescale) {
-          uint32_t ov[NH];
-          tmem_ld_n<NH>(tmem + lane_off + kOCol, ov);
-          tmem_ld_wait_n<NH>(ov);
+        if (t > 0 && heavy && rescale) {
+          uint32_t ov[16];
+          tmem_ld16(tmem + lane_off + kOCol, ov);
+          tmem_ld_wait_n<16>(ov);
 #pragma unroll
-          for (int h = 0; h < NH; ++h) ov[h] = __float_as_uint(__uint_as_float(ov[h]) * alpha[h]);
-          tmem_st_n<NH>(tmem + lane_off + kOCol, ov);
+          for (int c = 0; c < 16; ++c) ov[c] = __float_as_uint(__uint_as_float(ov[c]) * alpha_all[c]);
+          tmem_st16(tmem + lane_off + kOCol, ov);
           tmem_st_wait();
         }
         if (!valid) {
-          // this key's V row may hold another split's key, a stale tile or
-          // poison: P is 0 there, but 0 * NaN is not, so zero the row
+          // this row's V may hold another split's key, a stale tile or poison:
+          // P is 0 there, but 0 * NaN is not, so zero the row
           const uint32_t fill_v = 2u * g + 1u;
           const uint32_t sv_slot = fill_v % kSlots;
           if (!mbar_wait(bar_kv_full + 8u * sv_slot, (fill_v / kSlots) & 1, abort_flag)) { ok = false; break; }
-          uint8_t* vrow = smem + (sRing - base) + sv_slot * kTileBytes + r * 128;
+          uint8_t* vrow = smem + (sRing - base) + sv_slot * kTileBytes + grp16 * 4096 + (r & 15) * 128;
 #pragma unroll
           for (int c = 0; c < 8; ++c) {
             *reinterpret_cast<uint4*>(vrow + c * 16) = make_uint4(0u, 0u, 0u, 0u);
-            *reinterpret_cast<uint4*>(vrow + kHalfBytes + c * 16) = make_uint4(0u, 0u, 0u, 0u);
+            *reinterpret_cast<uint4*>(vrow + 2048 + c * 16) = make_uint4(0u, 0u, 0u, 0u);
           }
         }
         uint8_t* pb = smem + (sP - base) + (g & 1u) * kPBytes;
 #pragma unroll
-        for (int h = 0; h < NH; ++h) {
-          const uint16_t v = BF16 ? __bfloat16_as_ushort(__float2bfloat16_rn(pr[h]))
-                                  : __half_as_ushort(__float2half_rn(pr[h]));
-          *reinterpret_cast<uint16_t*>(pb + p_offset(h, r)) = v;
+        for (int j = 0; j < GH; ++j) {
+          const uint16_t v = BF16 ? __bfloat16_as_ushort(__float2bfloat16_rn(pr[j]))
+                                  : __half_as_ushort(__float2half_rn(pr[j]));
+          *reinterpret_cast<uint16_t*>(pb + p_offset(c0 + j, r)) = v;
         }
         fence_proxy_async_smem();
         tc_fence_before();
@@ -440,45 +569,47 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
       }
       if (!ok) break;
       // ---- item epilogue: denominators, then partial or final output
-      float o[NH];
+      float o[16];
       if (n_tiles > 0) {
         if (!mbar_wait(bar_pv_done, (g - 1) & 1, abort_flag)) { ok = false; break; }
         tc_fence_after();
-        uint32_t ov[NH];
-        tmem_ld_n<NH>(tmem + lane_off + kOCol, ov);
-        tmem_ld_wait_n<NH>(ov);
+        uint32_t ov[16];
+        tmem_ld16(tmem + lane_off + kOCol, ov);
+        tmem_ld_wait_n<16>(ov);
 #pragma unroll
-        for (int h = 0; h < NH; ++h) o[h] = __uint_as_float(ov[h]);
+        for (int c = 0; c < 16; ++c) o[c] = __uint_as_float(ov[c]);
       } else {
 #pragma unroll
-        for (int h = 0; h < NH; ++h) o[h] = 0.f;
+        for (int c = 0; c < 16; ++c) o[c] = 0.f;
       }
-      float* lb = lred + (red_uses & 1u) * 64;
+      float* lb = lred + (red_uses & 1u) * 128;
 #pragma unroll
-      for (int h = 0; h < NH; ++h) {
-        float v = lp[h];
+      for (int j = 0; j < GH; ++j) {
+        float v = lp[j];
 #pragma unroll
-        for (int off = 16; off >= 1; off >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, off);
-        if (lane == 0) lb[sw * 16 + h] = v;
+        for (int off = 8; off >= 1; off >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, off);
+        if ((lane & 15) == 0) lb[grp16 * 16 + j] = v;
       }
       if (!cta_sync()) { ok = false; break; }
-      const int h0 = e.hg * GH;
 #pragma unroll
-      for (int h = 0; h < NH; ++h) {
-        if (h >= GH) break;
-        const float L = (lb[h] + lb[16 + h]) + (lb[32 + h] + lb[48 + h]);
-        const int64_t row = (int64_t)e.b * Hq + h0 + h;
+      for (int c = 0; c < 16; ++c) {
+        if (c >= NC) break;
+        const int hh = c / GH, jj = c % GH;
+        float L = 0.f;
+        for (int gg = hh; gg < NG; gg += F) L += lb[gg * 16 + jj];
+        const int qh = (e.kvh0 + hh) * G + (e.q0 - e.kvh0 * G) + jj;
+        const int64_t row = (int64_t)e.b * Hq + qh;
         if (p.num_splits > 1) {
-          p.part_o[(row * p.num_splits + e.split) * kD + r] = o[h];
+          p.part_o[(row * p.num_splits + e.split) * kD + r] = o[c];
           if (r == 0) {
-            p.part_ml[(row * p.num_splits + e.split) * 2 + 0] = m[h];
+            p.part_ml[(row * p.num_splits + e.split) * 2 + 0] = mcol[c];
             p.part_ml[(row * p.num_splits + e.split) * 2 + 1] = L;
           }
         } else {
-          const float v = L > 0.f ? o[h] / L : 0.f;
+          const float v = L > 0.f ? o[c] / L : 0.f;
           if (p.rounding == 3) static_cast<float*>(p.out)[row * kD + r] = v;
           else static_cast<uint16_t*>(p.out)[row * kD + r] = round_out<BF16>(v, p.rounding);
-          if (r == 0 && p.lse) p.lse[row] = L > 0.f ? m[h] * kLn2 + logf(L) : -INFINITY;
+          if (r == 0 && p.lse) p.lse[row] = L > 0.f ? mcol[c] * kLn2 + logf(L) : -INFINITY;
         }
       }
     }
@@ -493,28 +624,40 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
   if (threadIdx.x == 0 && *abort_flag) report_status(p.status, kStatusTimeout);
 }
 
-template <bool BF16, int NH>
+template <bool BF16, int GH>
 cudaError_t launch_t(const DecodeParams& p, int grid, cudaStream_t stream) {
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<BF16, NH>,
+    cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<BF16, GH>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  decode_tc_kernel<BF16, NH><<<grid, kThreads, kSmemBytes, stream>>>(p);
+  decode_tc_kernel<BF16, GH><<<grid, kThreads, kSmemBytes, stream>>>(p);
   return cudaGetLastError();
+}
+
+template <bool BF16>
+cudaError_t launch_b(const DecodeParams& p, int grid, cudaStream_t stream) {
+  switch (p.heads_per_item) {
+    case 1: return launch_t<BF16, 1>(p, grid, stream);
+    case 2: return launch_t<BF16, 2>(p, grid, stream);
+    case 4: return launch_t<BF16, 4>(p, grid, stream);
+    case 8: return launch_t<BF16, 8>(p, grid, stream);
+    case 16: return launch_t<BF16, 16>(p, grid, stream);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 }  // namespace
 
-// Splits of one decode step on the tcgen05 path (head size 128, heads per
-// item <= 16).  The caller has zeroed p.counter on `stream`.
+// Splits of one decode step on the tcgen05 path (head size 128).  The caller
+// has chosen heads_per_item (query heads per KV head in an item: G, or 16
+// when G is a multiple of 16 above it; a power of two) and kv_per_item (F,
+// with F * heads_per_item <= 16 and F dividing num_kv_heads), encoded the
+// tensor maps and zeroed p.counter on `stream`.
 cudaError_t launch_decode_tc(const DecodeParams& p, bool bf16, int grid, cudaStream_t stream) {
-  const int gh = p.heads_per_item;
-  if (gh <= 4) return bf16 ? launch_t<true, 4>(p, grid, stream) : launch_t<false, 4>(p, grid, stream);
-  if (gh <= 8) return bf16 ? launch_t<true, 8>(p, grid, stream) : launch_t<false, 8>(p, grid, stream);
-  return bf16 ? launch_t<true, 16>(p, grid, stream) : launch_t<false, 16>(p, grid, stream);
+  return bf16 ? launch_b<true>(p, grid, stream) : launch_b<false>(p, grid, stream);
 }
 
 }  // namespace attn
