@@ -47,7 +47,9 @@ struct PrefillLayout {
   static constexpr int kBarOff = kRingOff + kStages * kTileBytes;
   static constexpr int kNumBars = 2 + 2 * kStages + 2 + 2 + 2 + 1;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
-  static constexpr int kSmemBytes = kMiscOff + 16 + 1024;  // + slack for 1024-byte alignment
+  // epilogue staging: 32 rows x 64 bytes per softmax warp (8 warps)
+  static constexpr int kStageOff = (kMiscOff + 16 + 127) / 128 * 128;
+  static constexpr int kSmemBytes = kStageOff + 8 * 2048 + 1024;  // + slack for 1024-byte alignment
   static __device__ __forceinline__ constexpr uint32_t s_col(int t) { return t ? 128u : 0u; }
   static __device__ __forceinline__ constexpr uint32_t o_col(int t) { return t ? 256u + D : 256u; }
   static constexpr uint32_t kTmemCols = 512;
@@ -212,46 +214,47 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       for (int t = 0; t < 2; ++t)
         if (n_kv[t] > 0) drain_wait(bar_q_full + 8u * t, 0);
     }
-  } else if (warp == 1) {
+  } else if (warp == 1 && lane == 0) {
     // ---------------------------------------------------------- MMA issuer
-    const bool leader = lane == 0;
+    // One thread: an MMA issue blocks for about one MMA's duration, so
+    // every other instruction on this thread is tensor-pipe idle time.  The
+    // shared-memory descriptors are built once; a K-step or a ring slot is
+    // a constant added to the 16-byte address field (addresses < 256 KB).
     const uint32_t idesc_s = make_idesc_f16(BF16, kBM, kBN, false);
     const uint32_t idesc_pv = make_idesc_f16(BF16, kBM, D, true);
+    const uint64_t dq0 = make_sdesc_sw128(sQ, 16, 1024);                  // Q_0, K-major
+    const uint64_t dk0 = make_sdesc_sw128(sRing, 16, 1024);               // K in slot 0, K-major
+    const uint64_t dv0 = make_sdesc_sw128(sRing, L::kHalfBytes, 1024);    // V in slot 0, MN-major
+    constexpr uint64_t kTileStep = L::kTileBytes >> 4;
     auto issue_s = [&](int t, int slot) {
-      const uint32_t a0 = sQ + t * L::kTileBytes;
-      const uint32_t b0 = sRing + slot * L::kTileBytes;
+      const uint64_t a = dq0 + (uint64_t)t * kTileStep;
+      const uint64_t b = dk0 + (uint64_t)slot * kTileStep;
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
-        const uint32_t o = (kk >> 2) * L::kHalfBytes + (kk & 3) * 32;
-        umma_ss(tmem + L::s_col(t), make_sdesc_sw128(a0 + o, 16, 1024),
-                make_sdesc_sw128(b0 + o, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
+        const uint64_t o = (uint64_t)(((kk >> 2) * L::kHalfBytes + (kk & 3) * 32) >> 4);
+        umma_ss(tmem + L::s_col(t), a + o, b + o, idesc_s, kk > 0 ? 1u : 0u);
       }
     };
     auto issue_pv = [&](int t, int slot, bool acc) {
-      const uint32_t b0 = sRing + slot * L::kTileBytes;
+      const uint64_t b = dv0 + (uint64_t)slot * kTileStep;
 #pragma unroll
-      for (int kk = 0; kk < kBN / 16; ++kk) {
-        umma_ts(tmem + L::o_col(t), tmem + L::s_col(t) + kk * 8,
-                make_sdesc_sw128(b0 + kk * 16 * 128, L::kHalfBytes, 1024), idesc_pv,
-                (acc || kk > 0) ? 1u : 0u);
-      }
+      for (int kk = 0; kk < kBN / 16; ++kk)
+        umma_ts(tmem + L::o_col(t), tmem + L::s_col(t) + kk * 8, b + (uint64_t)((kk * 16 * 128) >> 4),
+                idesc_pv, (acc || kk > 0) ? 1u : 0u);
     };
     bool ok = true;
     for (int t = 0; t < 2 && ok; ++t)
       if (n_kv[t] > 0) ok = mbar_wait(bar_q_full + 8u * t, 0, abort_flag);
     if (ok && n_kv_max > 0) {
-      ok = mbar_wait(bar_kv_full, 0, abort_flag);  // K_0: item 0, slot 0, first fill
+      ok = mbar_wait(bar_kv_full, 0, abort_flag);  // K_0: slot 0, first fill
       if (ok) {
         tc_fence_after();
         for (int t = 0; t < 2; ++t) {
           if (n_kv[t] == 0) continue;
-          if (leader) {
-            issue_s(t, 0);
-            umma_commit(bar_s_full + 8u * t);
-          }
+          issue_s(t, 0);
+          umma_commit(bar_s_full + 8u * t);
         }
-        if (leader) umma_commit(bar_kv_empty);
-        __syncwarp();
+        umma_commit(bar_kv_empty);
       }
     }
     for (int j = 0; ok && j < n_kv_max; ++j) {
@@ -264,7 +267,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         // anything (NaN included); P is 0 there but 0 * NaN is not, so zero them.
         const int r0 = Sk - j * kBN;
         uint8_t* vt = smem + (sRing - base) + sv * L::kTileBytes;
-        for (int idx = lane; idx < (kBN - r0) * L::kHalves * 8; idx += 32) {
+        for (int idx = 0; idx < (kBN - r0) * L::kHalves * 8; ++idx) {
           const int chunk = idx & 7;
           const int rh = idx >> 3;
           const int h = rh % L::kHalves;
@@ -273,7 +276,6 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
               make_uint4(0u, 0u, 0u, 0u);
         }
         fence_proxy_async_smem();
-        __syncwarp();
       }
       bool k_next = false;
       int sk_next = 0;
@@ -281,7 +283,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         if (j >= n_kv[t]) continue;
         if (!mbar_wait(bar_p_full + 8u * t, j & 1, abort_flag)) { ok = false; break; }
         tc_fence_after();
-        if (leader) issue_pv(t, sv, j > 0);
+        issue_pv(t, sv, j > 0);
         if (j + 1 < n_kv[t]) {
           if (!k_next) {
             const int ik = 2 * (j + 1);
@@ -293,24 +295,17 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
             tc_fence_after();
             k_next = true;
           }
-          if (leader) {
-            issue_s(t, sk_next);
-            umma_commit(bar_s_full + 8u * t);
-          }
-        } else if (leader) {
+          issue_s(t, sk_next);
+          umma_commit(bar_s_full + 8u * t);
+        } else {
           umma_commit(bar_o_full + 8u * t);
         }
-        __syncwarp();
       }
-      if (leader) {
-        umma_commit(bar_kv_empty + 8u * sv);
-        if (k_next) umma_commit(bar_kv_empty + 8u * sk_next);
-      }
-      __syncwarp();
+      umma_commit(bar_kv_empty + 8u * sv);
+      if (k_next) umma_commit(bar_kv_empty + 8u * sk_next);
     }
     // no MMA may still be running when TMEM is released
-    if (leader) umma_commit(bar_mma_done);
-    __syncwarp();
+    umma_commit(bar_mma_done);
     drain_wait(bar_mma_done, 0);
   } else if (warp >= 4) {
     // ---------------------------------------------------------- softmax + epilogue
@@ -341,12 +336,18 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
           for (int e = 0; e < 32; ++e)
             if (32 * c + e >= cl) s[c][e] = 0xFF800000u;  // -inf
       }
-      // row max over the tile's 128 scores (three-input max: 1 + 63 steps + 1)
-      float mx = __uint_as_float(s[0][0]);
+      // row max over the tile's 128 scores: four independent chains of
+      // three-input maxima (one per 32-column chunk), then one merge
+      float mc[4];
 #pragma unroll
-      for (int i = 1; i + 1 < 128; i += 2)
-        mx = fmax3(mx, __uint_as_float(s[i >> 5][i & 31]), __uint_as_float(s[(i + 1) >> 5][(i + 1) & 31]));
-      mx = fmaxf(mx, __uint_as_float(s[3][31]));
+      for (int c = 0; c < 4; ++c) mc[c] = __uint_as_float(s[c][0]);
+#pragma unroll
+      for (int i = 1; i + 1 < 32; i += 2)
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          mc[c] = fmax3(mc[c], __uint_as_float(s[c][i]), __uint_as_float(s[c][i + 1]));
+      const float mx = fmax3(fmaxf(mc[0], __uint_as_float(s[0][31])), fmaxf(mc[1], __uint_as_float(s[1][31])),
+                             fmax3(mc[2], mc[3], fmaxf(__uint_as_float(s[2][31]), __uint_as_float(s[3][31]))));
       // The running max is only raised when the tile's max exceeds it by
       // more than kRescaleSlack (log2 units).  Any reference value works for
       // the recurrence as long as o and l use the same one, so this is exact;
@@ -357,7 +358,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       const float alpha = fast_exp2(m - m_use);
       const float2 sc2 = make_float2(sl2, sl2);
       const float2 nm2 = make_float2(-m_use, -m_use);
-      float2 rs2 = make_float2(0.f, 0.f);
+      float2 rs[4];
+#pragma unroll
+      for (int a = 0; a < 4; ++a) rs[a] = make_float2(0.f, 0.f);
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t pk[16];
@@ -366,12 +369,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
           const float2 x = ffma2(make_float2(__uint_as_float(s[c][2 * e]), __uint_as_float(s[c][2 * e + 1])),
                                  sc2, nm2);
           const float2 pp = make_float2(fast_exp2(x.x), fast_exp2(x.y));
-          rs2 = fadd2(rs2, pp);
+          rs[e & 3] = fadd2(rs[e & 3], pp);
           pk[e] = BF16 ? pack_bf16x2_rn(pp.x, pp.y) : pack_f16x2_rn(pp.x, pp.y);
         }
         tmem_st16(tS + 16 * c, pk);
       }
-      l = l * alpha + (rs2.x + rs2.y);
       if (j > 0 && __any_sync(0xFFFFFFFFu, alpha != 1.f)) {
         // O_t is final for tile j-1 here: S_t(j) was issued after PV_t(j-1)
         // and its commit covers every earlier MMA.
@@ -393,6 +395,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(bar_p_full + 8u * t);
+      const float2 r01 = fadd2(rs[0], rs[1]), r23 = fadd2(rs[2], rs[3]);
+      l = l * alpha + ((r01.x + r23.x) + (r01.y + r23.y));
       m = m_new;
     }
     if (ok && n_kv[t] > 0) {
@@ -402,8 +406,30 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     if (ok) {
       const bool row_ok = r < rows[t];
       const int64_t tok = (int64_t)q_begin + row0[t] + r;
-      const int64_t obase = (tok * p.num_q_heads + head[t]) * D;
       const float inv_l = l > 0.f ? 1.f / l : 0.f;
+      // The warp writes its 32 rows through a 2 KB staging buffer so that
+      // each store instruction covers 8 rows x 64 contiguous bytes instead of
+      // 32 rows x 16 bytes.  Row i of the buffer holds 64 bytes of row i, its
+      // four 16-byte pieces rotated by (i & 3) to spread the banks.
+      uint8_t* stage = smem + L::kStageOff + (warp - 4) * 2048;
+      const int64_t row_elems = (int64_t)p.num_q_heads * D;
+      const int64_t tile_base = ((int64_t)q_begin + row0[t] + wq * 32) * row_elems + (int64_t)head[t] * D;
+      const int rows_here = min(32, rows[t] - wq * 32);   // valid rows of this warp
+      auto flush = [&](int64_t col_byte) {                // write 64 bytes per row
+        __syncwarp();
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int rr = 8 * k + (lane >> 2), piece = lane & 3;
+          const uint4 v = *reinterpret_cast<const uint4*>(stage + rr * 64 + ((piece ^ (rr & 3)) * 16));
+          if (rr < rows_here) {
+            uint8_t* g = reinterpret_cast<uint8_t*>(p.out) +
+                         (tile_base + (int64_t)rr * row_elems) * (p.rounding == 3 ? 4 : 2) + col_byte +
+                         piece * 16;
+            *reinterpret_cast<uint4*>(g) = v;
+          }
+        }
+        __syncwarp();
+      };
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
         uint32_t o[32];
@@ -414,22 +440,29 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
 #pragma unroll
           for (int e = 0; e < 32; ++e) o[e] = 0u;
         }
-        if (!row_ok) continue;
         if (p.rounding == 3) {
-          float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + obase + 32 * c);
 #pragma unroll
-          for (int v = 0; v < 8; ++v)
-            dst[v] = make_float4(__uint_as_float(o[4 * v]) * inv_l, __uint_as_float(o[4 * v + 1]) * inv_l,
-                                 __uint_as_float(o[4 * v + 2]) * inv_l, __uint_as_float(o[4 * v + 3]) * inv_l);
+          for (int hlf = 0; hlf < 2; ++hlf) {
+#pragma unroll
+            for (int v = 0; v < 4; ++v)
+              *reinterpret_cast<float4*>(stage + lane * 64 + ((v ^ (lane & 3)) * 16)) =
+                  make_float4(__uint_as_float(o[16 * hlf + 4 * v]) * inv_l,
+                              __uint_as_float(o[16 * hlf + 4 * v + 1]) * inv_l,
+                              __uint_as_float(o[16 * hlf + 4 * v + 2]) * inv_l,
+                              __uint_as_float(o[16 * hlf + 4 * v + 3]) * inv_l);
+            flush((int64_t)(32 * c + 16 * hlf) * 4);
+          }
         } else {
-          uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + obase + 32 * c);
-          uint32_t w[16];
+          uint32_t wv[16];
 #pragma unroll
           for (int e = 0; e < 16; ++e)
-            w[e] = round_out_x2<BF16>(__uint_as_float(o[2 * e]) * inv_l,
-                                      __uint_as_float(o[2 * e + 1]) * inv_l, p.rounding);
+            wv[e] = round_out_x2<BF16>(__uint_as_float(o[2 * e]) * inv_l,
+                                       __uint_as_float(o[2 * e + 1]) * inv_l, p.rounding);
 #pragma unroll
-          for (int v = 0; v < 4; ++v) dst[v] = make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
+          for (int v = 0; v < 4; ++v)
+            *reinterpret_cast<uint4*>(stage + lane * 64 + ((v ^ (lane & 3)) * 16)) =
+                make_uint4(wv[4 * v], wv[4 * v + 1], wv[4 * v + 2], wv[4 * v + 3]);
+          flush((int64_t)(32 * c) * 2);
         }
       }
       if (row_ok && p.lse)
