@@ -242,25 +242,30 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         umma_ts(tmem + L::o_col(t), tmem + L::s_col(t) + kk * 8, b + (uint64_t)((kk * 16 * 128) >> 4),
                 idesc_pv, (acc || kk > 0) ? 1u : 0u);
     };
+    const int nk0 = n_kv[0], nk1 = n_kv[1];
     bool ok = true;
-    for (int t = 0; t < 2 && ok; ++t)
-      if (n_kv[t] > 0) ok = mbar_wait(bar_q_full + 8u * t, 0, abort_flag);
+    if (nk0 > 0) ok = mbar_wait(bar_q_full, 0, abort_flag);
+    if (ok && nk1 > 0) ok = mbar_wait(bar_q_full + 8u, 0, abort_flag);
     if (ok && n_kv_max > 0) {
       ok = mbar_wait(bar_kv_full, 0, abort_flag);  // K_0: slot 0, first fill
       if (ok) {
         tc_fence_after();
-        for (int t = 0; t < 2; ++t) {
-          if (n_kv[t] == 0) continue;
-          issue_s(t, 0);
-          umma_commit(bar_s_full + 8u * t);
+        if (nk0 > 0) {
+          issue_s(0, 0);
+          umma_commit(bar_s_full);
+        }
+        if (nk1 > 0) {
+          issue_s(1, 0);
+          umma_commit(bar_s_full + 8u);
         }
         umma_commit(bar_kv_empty);
       }
     }
+    // per key tile j: PV_0(j), S_0(j+1), PV_1(j), S_1(j+1)
     for (int j = 0; ok && j < n_kv_max; ++j) {
-      const int iv = 2 * j + 1;
+      const int iv = 2 * j + 1;                    // V_j
       const int sv = iv % L::kStages;
-      if (!mbar_wait(bar_kv_full + 8u * sv, (iv / L::kStages) & 1, abort_flag)) { ok = false; break; }
+      if (!mbar_wait(bar_kv_full + 8u * sv, (iv / L::kStages) & 1, abort_flag)) break;
       tc_fence_after();
       if ((j + 1) * kBN > Sk) {
         // keys at or past kv_len in the last tile: their V rows may hold
@@ -277,32 +282,39 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         }
         fence_proxy_async_smem();
       }
-      bool k_next = false;
-      int sk_next = 0;
-      for (int t = 0; t < 2 && ok; ++t) {
-        if (j >= n_kv[t]) continue;
-        if (!mbar_wait(bar_p_full + 8u * t, j & 1, abort_flag)) { ok = false; break; }
+      const int ik = iv + 1;                       // K_{j+1}
+      const int sk = ik % L::kStages;
+      const bool s0 = j + 1 < nk0, s1 = j + 1 < nk1;
+      if (j < nk0) {
+        if (!mbar_wait(bar_p_full, j & 1, abort_flag)) break;
         tc_fence_after();
-        issue_pv(t, sv, j > 0);
-        if (j + 1 < n_kv[t]) {
-          if (!k_next) {
-            const int ik = 2 * (j + 1);
-            sk_next = ik % L::kStages;
-            if (!mbar_wait(bar_kv_full + 8u * sk_next, (ik / L::kStages) & 1, abort_flag)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            k_next = true;
-          }
-          issue_s(t, sk_next);
-          umma_commit(bar_s_full + 8u * t);
+        issue_pv(0, sv, j > 0);
+      }
+      if (s0 || s1) {
+        if (!mbar_wait(bar_kv_full + 8u * sk, (ik / L::kStages) & 1, abort_flag)) break;
+        tc_fence_after();
+      }
+      if (j < nk0) {
+        if (s0) {
+          issue_s(0, sk);
+          umma_commit(bar_s_full);
         } else {
-          umma_commit(bar_o_full + 8u * t);
+          umma_commit(bar_o_full);
+        }
+      }
+      if (j < nk1) {
+        if (!mbar_wait(bar_p_full + 8u, j & 1, abort_flag)) break;
+        tc_fence_after();
+        issue_pv(1, sv, j > 0);
+        if (s1) {
+          issue_s(1, sk);
+          umma_commit(bar_s_full + 8u);
+        } else {
+          umma_commit(bar_o_full + 8u);
         }
       }
       umma_commit(bar_kv_empty + 8u * sv);
-      if (k_next) umma_commit(bar_kv_empty + 8u * sk_next);
+      if (s0 || s1) umma_commit(bar_kv_empty + 8u * sk);
     }
     // no MMA may still be running when TMEM is released
     umma_commit(bar_mma_done);
@@ -311,16 +323,23 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     // ---------------------------------------------------------- softmax + epilogue
     const int t = (warp - 4) >> 2;
     const int wq = warp & 3;
+    // this tile's bounds as scalars (a runtime index into the arrays would
+    // put them in local memory)
+    const int t_row0 = t ? row0[1] : row0[0];
+    const int t_rows = t ? rows[1] : rows[0];
+    const int t_nkv = t ? n_kv[1] : n_kv[0];
+    const int t_limlo = t ? lim_lo[1] : lim_lo[0];
+    const int t_head = t ? head[1] : head[0];
     const int r = wq * 32 + lane;
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
     const uint32_t tS = tmem + lane_off + L::s_col(t);
     const uint32_t tO = tmem + lane_off + L::o_col(t);
-    const int i_row = row0[t] + r;
+    const int i_row = t_row0 + r;
     const int key_lim = p.causal ? min(Sk, i_row + off + 1) : Sk;
     const float sl2 = p.scale_log2;
     float m = -INFINITY, l = 0.f;
     bool ok = true;
-    for (int j = 0; j < n_kv[t]; ++j) {
+    for (int j = 0; j < t_nkv; ++j) {
       if (!mbar_wait(bar_s_full + 8u * t, j & 1, abort_flag)) { ok = false; break; }
       tc_fence_after();
       uint32_t s[4][32];
@@ -328,7 +347,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       for (int c = 0; c < 4; ++c) tmem_ld32(tS + 32 * c, s[c]);
 #pragma unroll
       for (int c = 0; c < 4; ++c) tmem_ld_wait(s[c]);
-      if ((j + 1) * kBN > lim_lo[t]) {
+      if ((j + 1) * kBN > t_limlo) {
         const int cl = key_lim - j * kBN;  // columns >= cl are masked for this row
 #pragma unroll
         for (int c = 0; c < 4; ++c)
@@ -399,13 +418,13 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       l = l * alpha + ((r01.x + r23.x) + (r01.y + r23.y));
       m = m_new;
     }
-    if (ok && n_kv[t] > 0) {
+    if (ok && t_nkv > 0) {
       ok = mbar_wait(bar_o_full + 8u * t, 0, abort_flag);
       tc_fence_after();
     }
     if (ok) {
-      const bool row_ok = r < rows[t];
-      const int64_t tok = (int64_t)q_begin + row0[t] + r;
+      const bool row_ok = r < t_rows;
+      const int64_t tok = (int64_t)q_begin + t_row0 + r;
       const float inv_l = l > 0.f ? 1.f / l : 0.f;
       // The warp writes its 32 rows through a 2 KB staging buffer so that
       // each store instruction covers 8 rows x 64 contiguous bytes instead of
@@ -413,8 +432,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       // four 16-byte pieces rotated by (i & 3) to spread the banks.
       uint8_t* stage = smem + L::kStageOff + (warp - 4) * 2048;
       const int64_t row_elems = (int64_t)p.num_q_heads * D;
-      const int64_t tile_base = ((int64_t)q_begin + row0[t] + wq * 32) * row_elems + (int64_t)head[t] * D;
-      const int rows_here = min(32, rows[t] - wq * 32);   // valid rows of this warp
+      const int64_t tile_base = ((int64_t)q_begin + t_row0 + wq * 32) * row_elems + (int64_t)t_head * D;
+      const int rows_here = min(32, t_rows - wq * 32);   // valid rows of this warp
       auto flush = [&](int64_t col_byte) {                // write 64 bytes per row
         __syncwarp();
 #pragma unroll
@@ -433,7 +452,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
         uint32_t o[32];
-        if (n_kv[t] > 0) {
+        if (t_nkv > 0) {
           tmem_ld32(tO + 32 * c, o);
           tmem_ld_wait(o);
         } else {
@@ -466,7 +485,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         }
       }
       if (row_ok && p.lse)
-        p.lse[tok * p.num_q_heads + head[t]] = l > 0.f ? m * kLn2 + logf(l) : -INFINITY;
+        p.lse[tok * p.num_q_heads + t_head] = l > 0.f ? m * kLn2 + logf(l) : -INFINITY;
     }
   }
 
