@@ -220,6 +220,10 @@ attn_status_t attn_fwd_prefill(void* out, const void* q, const void* k_cache, co
     const cuuint64_t strides[2] = {d * 2, d * 2 * (cuuint64_t)num_q_heads};
     const cuuint32_t box[3] = {64, 1, 128};
     if (!attn::encode_tiled(&p.tm_q, bf16, 3, dims, strides, box, q, CU_TENSOR_MAP_SWIZZLE_128B)) return ATTN_ERR_CUDA;
+    // full 128-row output tiles are stored through a map of the same shape
+    if (rounding != ATTN_OUT_F32 &&
+        !attn::encode_tiled(&p.tm_o, bf16, 3, dims, strides, box, out, CU_TENSOR_MAP_SWIZZLE_128B))
+      return ATTN_ERR_CUDA;
   }
   {
     const cuuint64_t dims[4] = {d, (cuuint64_t)num_kv_heads, (cuuint64_t)block_size,

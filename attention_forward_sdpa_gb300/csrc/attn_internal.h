@@ -14,6 +14,7 @@ struct PrefillParams {
   CUtensorMap tm_q;   // Q  [total_q, Hq, d]: dims (d, Hq, total_q), box (64, 1, 128), 128B swizzle
   CUtensorMap tm_k;   // K  [num_blocks, bs, Hkv, d]: dims (d, Hkv, bs, num_blocks), box (64, 1, R, 1)
   CUtensorMap tm_v;   // V  same as K
+  CUtensorMap tm_o;   // O  like Q over the output (16-bit output only)
   void* out;          // [total_q, Hq, d] 16-bit, or fp32 when rounding == 3
   float* lse;         // [total_q, Hq] or nullptr
   int32_t* status;    // device status word or nullptr

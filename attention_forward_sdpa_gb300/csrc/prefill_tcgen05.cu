@@ -422,10 +422,55 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       ok = mbar_wait(bar_o_full + 8u * t, 0, abort_flag);
       tc_fence_after();
     }
-    if (ok) {
-      const bool row_ok = r < t_rows;
-      const int64_t tok = (int64_t)q_begin + t_row0 + r;
-      const float inv_l = l > 0.f ? 1.f / l : 0.f;
+    const bool row_ok = r < t_rows;
+    const int64_t tok = (int64_t)q_begin + t_row0 + r;
+    const float inv_l = l > 0.f ? 1.f / l : 0.f;
+    if (t_rows == kBM && p.rounding != 3) {
+      // Full tile, 16-bit output: the rows are written into this tile's Q
+      // slot (free: the o_full commit covers every product that read it) in
+      // the 128-byte-swizzled layout of the Q map, and one thread stores the
+      // tile with TMA.  All 128 threads reach the barrier, whatever ok says.
+      if (ok) {
+        uint8_t* qt = smem + L::kQOff + t * L::kTileBytes;
+        // two 32-column chunks per TMEM round trip
+#pragma unroll
+        for (int c2 = 0; c2 < D / 64; ++c2) {
+          uint32_t o[2][32];
+          if (t_nkv > 0) {
+            tmem_ld32(tO + 64 * c2, o[0]);
+            tmem_ld32(tO + 64 * c2 + 32, o[1]);
+            tmem_ld_wait(o[0]);
+            tmem_ld_wait(o[1]);
+          } else {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[0][e] = o[1][e] = 0u;
+          }
+#pragma unroll
+          for (int hc = 0; hc < 2; ++hc) {
+            uint32_t w[16];
+            round_pack32<BF16>(o[hc], inv_l, p.rounding, w);
+            // columns [64 c2 + 32 hc, +32): half c2, 16-byte chunks 4 hc .. 4 hc + 3
+            uint8_t* rowp = qt + c2 * L::kHalfBytes + r * 128;
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              const int chunk = hc * 4 + v;
+              *reinterpret_cast<uint4*>(rowp + ((chunk ^ (r & 7)) * 16)) =
+                  make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
+            }
+          }
+        }
+      }
+      fence_proxy_async_smem();
+      named_bar_sync(1 + t, kBM);
+      if (wq == 0 && lane == 0 && ok && *abort_flag == 0) {
+#pragma unroll
+        for (int h = 0; h < L::kHalves; ++h)
+          tma_store_3d(&p.tm_o, sQ + t * L::kTileBytes + h * L::kHalfBytes, h * 64, t_head,
+                       q_begin + t_row0);
+        bulk_commit_group();
+        bulk_wait_group_read0();
+      }
+    } else if (ok) {
       // The warp writes its 32 rows through a 2 KB staging buffer so that
       // each store instruction covers 8 rows x 64 contiguous bytes instead of
       // 32 rows x 16 bytes.  Row i of the buffer holds 64 bytes of row i, its
@@ -473,10 +518,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
           }
         } else {
           uint32_t wv[16];
-#pragma unroll
-          for (int e = 0; e < 16; ++e)
-            wv[e] = round_out_x2<BF16>(__uint_as_float(o[2 * e]) * inv_l,
-                                       __uint_as_float(o[2 * e + 1]) * inv_l, p.rounding);
+          round_pack32<BF16>(o, inv_l, p.rounding, wv);
 #pragma unroll
           for (int v = 0; v < 4; ++v)
             *reinterpret_cast<uint4*>(stage + lane * 64 + ((v ^ (lane & 3)) * 16)) =
@@ -484,9 +526,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
           flush((int64_t)(32 * c) * 2);
         }
       }
-      if (row_ok && p.lse)
-        p.lse[tok * p.num_q_heads + t_head] = l > 0.f ? m * kLn2 + logf(l) : -INFINITY;
     }
+    if (ok && row_ok && p.lse)
+      p.lse[tok * p.num_q_heads + t_head] = l > 0.f ? m * kLn2 + logf(l) : -INFINITY;
   }
 
   tc_fence_before();

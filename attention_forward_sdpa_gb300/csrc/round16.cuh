@@ -57,4 +57,56 @@ __device__ __forceinline__ uint32_t round_out_x2(float lo, float hi, int mode) {
   return (uint32_t)round_out<BF16>(lo, mode) | ((uint32_t)round_out<BF16>(hi, mode) << 16);
 }
 
+// 32 fp32 accumulator columns times scale -> 16 packed 16-bit pairs (even
+// column in the low half), with the mode tested once for the whole row chunk.
+// RTNE and RTZ use the packed conversions; bf16 RTNA adds half of the dropped
+// unit to the binary32 pattern (NaN kept quiet), fp16 RTNA takes the scalar
+// path above.
+template <bool BF16>
+__device__ __forceinline__ uint32_t cvt_pack_rn(float lo, float hi) {
+  uint32_t r;
+  if constexpr (BF16) asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  else asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+template <bool BF16>
+__device__ __forceinline__ uint32_t cvt_pack_rz(float lo, float hi) {
+  uint32_t r;
+  if constexpr (BF16) asm("cvt.rz.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  else asm("cvt.rz.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t bf16_rna_bits(float x) {
+  const uint32_t u = __float_as_uint(x);
+  const uint32_t nan = (u >> 16) | 0x0040u;
+  const uint32_t rounded = (u + 0x8000u) >> 16;
+  return (u & 0x7FFFFFFFu) > 0x7F800000u ? nan : rounded;
+}
+
+template <bool BF16>
+__device__ __forceinline__ void round_pack32(const uint32_t (&o)[32], float scale, int mode,
+                                             uint32_t (&w)[16]) {
+  if (mode == kRTNE) {
+#pragma unroll
+    for (int e = 0; e < 16; ++e)
+      w[e] = cvt_pack_rn<BF16>(__uint_as_float(o[2 * e]) * scale, __uint_as_float(o[2 * e + 1]) * scale);
+  } else if (mode == kRTZ) {
+#pragma unroll
+    for (int e = 0; e < 16; ++e)
+      w[e] = cvt_pack_rz<BF16>(__uint_as_float(o[2 * e]) * scale, __uint_as_float(o[2 * e + 1]) * scale);
+  } else if constexpr (BF16) {
+#pragma unroll
+    for (int e = 0; e < 16; ++e)
+      w[e] = bf16_rna_bits(__uint_as_float(o[2 * e]) * scale) |
+             (bf16_rna_bits(__uint_as_float(o[2 * e + 1]) * scale) << 16);
+  } else {
+#pragma unroll
+    for (int e = 0; e < 16; ++e)
+      w[e] = round_out_x2<false>(__uint_as_float(o[2 * e]) * scale, __uint_as_float(o[2 * e + 1]) * scale,
+                                 kRTNA);
+  }
+}
+
 }  // namespace attn
