@@ -291,25 +291,65 @@ __global__ void __launch_bounds__(kDecWarps * 32) decode_split_kernel(const __gr
 // units), summed in split order.  One warp per (sequence, q head).
 template <int D, bool BF16>
 __global__ void __launch_bounds__(128) decode_combine_kernel(const __grid_constant__ DecodeParams p) {
-  constexpr int DPL = D / 32;
+  constexpr int DPL = D / 32;                   // channels per lane: 4 at d = 128, 2 at d = 64
   const int lane = threadIdx.x & 31;
   const int64_t row = (int64_t)blockIdx.x * 4 + (threadIdx.x >> 5);
   if (row >= (int64_t)p.num_seqs * p.num_q_heads) return;
-  const int S = p.num_splits;
+  const int S = p.num_splits;                   // at most 64
+  // Lane s holds the (m, l) of split s and of split s + 32: one memory round
+  // trip for all of them; the max and the weight sum are warp reductions
+  // (every lane ends with the same values).
   const float* ml = p.part_ml + row * S * 2;
-  float M = -INFINITY;
-  for (int s = 0; s < S; ++s) M = fmaxf(M, ml[2 * s]);
+  float m_a = -INFINITY, l_a = 0.f, m_b = -INFINITY, l_b = 0.f;
+  if (lane < S) {
+    const float2 v = *reinterpret_cast<const float2*>(ml + 2 * lane);
+    m_a = v.x;
+    l_a = v.y;
+  }
+  if (lane + 32 < S) {
+    const float2 v = *reinterpret_cast<const float2*>(ml + 2 * (lane + 32));
+    m_b = v.x;
+    l_b = v.y;
+  }
+  float M = fmaxf(m_a, m_b);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, o));
   const float Mu = M == -INFINITY ? 0.f : M;
+  const float w_a = fast_exp2(m_a - Mu), w_b = fast_exp2(m_b - Mu);   // 0 for empty splits
+  float L = w_a * l_a + w_b * l_b;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xFFFFFFFFu, L, o);
+  // The partial rows, eight splits' loads in flight at a time, accumulated
+  // in split order.
   float acc[DPL];
 #pragma unroll
   for (int e = 0; e < DPL; ++e) acc[e] = 0.f;
-  float L = 0.f;
   const float* po = p.part_o + row * S * D + lane * DPL;
-  for (int s = 0; s < S; ++s) {
-    const float wgt = fast_exp2(ml[2 * s] - Mu);
-    L = fmaf(wgt, ml[2 * s + 1], L);
+  for (int s0 = 0; s0 < S; s0 += 8) {
+    float v[8][DPL];
+    float wg[8];
 #pragma unroll
-    for (int e = 0; e < DPL; ++e) acc[e] = fmaf(wgt, po[s * D + e], acc[e]);
+    for (int u = 0; u < 8; ++u) {
+      const int sp = s0 + u;
+      const float w = __shfl_sync(0xFFFFFFFFu, sp < 32 ? w_a : w_b, sp & 31);
+      wg[u] = sp < S ? w : 0.f;
+      if (sp < S) {
+        if constexpr (DPL == 4) {
+          const float4 x = *reinterpret_cast<const float4*>(po + (int64_t)sp * D);
+          v[u][0] = x.x; v[u][1] = x.y; v[u][2] = x.z; v[u][3] = x.w;
+        } else {
+          const float2 x = *reinterpret_cast<const float2*>(po + (int64_t)sp * D);
+          v[u][0] = x.x; v[u][1] = x.y;
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < DPL; ++e) v[u][e] = 0.f;
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+#pragma unroll
+      for (int e = 0; e < DPL; ++e) acc[e] = fmaf(wg[u], v[u][e], acc[e]);
   }
   const float inv = L > 0.f ? 1.f / L : 0.f;
 #pragma unroll

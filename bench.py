@@ -281,6 +281,13 @@ def run_ours(args, rank, world, dev):
     if not args.no_e2e:
         e2e = measure_e2e(args, pp, dp, dev, stream, attn, ws, world)
 
+    graph = None
+    if not args.no_graph:
+        try:
+            graph = measure_graph(pp, dp, pt, dt, p_out, d_out, ws, flush, attn, dev)
+        except Exception as exc:  # reported, never fatal: the eager numbers stand
+            graph = {"error": f"{type(exc).__name__}: {exc}"[:200]}
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(pp, dp, args.cpu_seconds)
@@ -303,10 +310,68 @@ def run_ours(args, rank, world, dev):
         "gpu_launches": K * 3,
         "clocks": clocks,
         "e2e": e2e,
+        "graph": graph,
         "cpu_baseline": cpu,
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
+
+
+def measure_graph(pp, dp, pt, dt, p_out, d_out, ws, flush, attn, dev, n=50):
+    """CUDA-graph replay of one call (kernel-only launch path): each call is
+    captured once on a side stream and replayed with the 256 MiB L2 flush
+    outside the graph; medians of n replays, CUDA events on the replay stream.
+    Also the small causal fp16 S=128 d=64 case, whose time is launch cost."""
+    c1 = attn_inputs.workload("prefill_causal_fp16_s128_d64")
+    c1t = device_args(c1, dev)
+    c1_out = torch.empty_like(c1t["q"])
+    cap = torch.cuda.Stream(dev)
+
+    def prefill(s):
+        attn.attn_fwd_prefill(p_out, pt["q"], pt["k_cache"], pt["v_cache"], pt["block_table"],
+                              pt["query_start_loc"], pt["seq_lens"], max_seqlen_q=pp.max_seqlen_q,
+                              max_seqlen_k=pp.max_seqlen_k, scale=pp.scale, causal=True, stream=s)
+
+    def decode(s):
+        attn.attn_fwd_decode(d_out, dt["q"], dt["k_cache"], dt["v_cache"], dt["block_table"],
+                             dt["seq_lens"], max_seqlen_k=dp.max_seqlen_k, scale=dp.scale,
+                             num_splits=DECODE_SPLITS, workspace=ws, stream=s)
+
+    def small(s):
+        attn.attn_fwd_prefill(c1_out, c1t["q"], c1t["k_cache"], c1t["v_cache"], c1t["block_table"],
+                              c1t["query_start_loc"], c1t["seq_lens"], max_seqlen_q=c1.max_seqlen_q,
+                              max_seqlen_k=c1.max_seqlen_k, scale=c1.scale, causal=True, stream=s)
+
+    cap.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(cap):
+        for fn in (prefill, decode, small):   # first calls (one-time setup) outside any capture
+            fn(cap)
+    torch.cuda.synchronize(dev)
+    graphs = {}
+    for name, fn in (("prefill", prefill), ("decode", decode), ("small_prefill", small)):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=cap):
+            fn(cap)
+        graphs[name] = g
+    torch.cuda.synchronize(dev)
+    cur = torch.cuda.current_stream(dev)
+    res = {}
+    for name, g in graphs.items():
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(n)]
+        for a, b in evs:
+            flush.zero_()
+            a.record(cur)
+            g.replay()
+            b.record(cur)
+        torch.cuda.synchronize(dev)
+        res[name] = statistics.median(a.elapsed_time(b) for a, b in evs) * 1e3
+    flops, dbytes = prefill_flops(pp), decode_bytes(dp)
+    return {"prefill_us": res["prefill"], "prefill_tflops": flops / res["prefill"] / 1e6,
+            "decode_us": res["decode"], "decode_gbs": dbytes / res["decode"] / 1e3,
+            "small_prefill_us": res["small_prefill"],
+            "small_prefill_workload": "prefill_causal_fp16_s128_d64",
+            "note": "median of %d graph replays, L2 flushed before each (outside the graph)" % n}
 
 
 def measure_e2e(args, pp, dp, dev, stream, attn, ws, world):
@@ -494,6 +559,7 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-graph", action="store_true", help="skip the CUDA-graph replay timings")
     ap.add_argument("--cpu-seconds", type=float, default=16.0)
     ap.add_argument("--ref-rows", type=int, default=128)
     args = ap.parse_args()
