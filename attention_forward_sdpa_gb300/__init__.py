@@ -66,6 +66,9 @@ def load_library() -> ctypes.CDLL:
         lib.attn_fwd_prefill.argtypes = [P, P, P, P, P, i32, P, P, i32, i32, i32, i32, i32, i32,
                                          i32, i32, i32, f32, i32, ctypes.c_int, ctypes.c_int, P,
                                          P, P]
+        lib.attn_fwd_dense.restype = ctypes.c_int
+        lib.attn_fwd_dense.argtypes = [P, P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, f32,
+                                       i32, ctypes.c_int, ctypes.c_int, P, P, P]
         lib.attn_decode_workspace_size.restype = sz
         lib.attn_decode_workspace_size.argtypes = [i32, i32, i32, i32]
         lib.attn_fwd_decode.restype = ctypes.c_int
@@ -179,6 +182,45 @@ def attn_fwd_prefill(out, q, k_cache, v_cache, block_table, query_start_loc, seq
     _check(rc, "attn_fwd_prefill")
 
 
+def _strides3(t, name):
+    """(batch, sequence, head) element strides of a logical [B, S, H, d] view,
+    which may be a permuted view (for instance BHSD memory seen as BSHD)."""
+    if t.dim() != 4:
+        raise ValueError(f"{name} must be 4-D [batch, seq, heads, head_size]")
+    if t.stride(3) != 1:
+        raise ValueError(f"{name}: the head_size dimension must be contiguous")
+    return (ctypes.c_int64 * 3)(t.stride(0), t.stride(1), t.stride(2))
+
+
+def attn_fwd_dense(out, q, k, v, *, scale: float, causal: bool, rounding: int = RTNE, lse=None,
+                   status=None, stream=None) -> None:
+    """Calls attn_fwd_dense on logical [batch, seq, heads, head_size] CUDA
+    tensors in any (batch, seq, head) stride order: BSHD tensors as they are,
+    BHSD tensors x as x.transpose(1, 2) (a view, nothing is copied)."""
+    lib = load_library()
+    dt = _dtype_code(q.dtype)
+    for t, name, want in ((q, "q", None), (k, "k", q.dtype), (v, "v", q.dtype),
+                          (out, "out", torch.float32 if rounding == OUT_F32 else q.dtype)):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor")
+        if want is not None and t.dtype != want:
+            raise TypeError(f"{name} must be {want}, got {t.dtype}")
+    if lse is not None:
+        _dev(lse, "lse", torch.float32)
+    if status is not None:
+        _dev(status, "status", torch.int32)
+    qs, ks, vs, os_ = (_strides3(q, "q"), _strides3(k, "k"), _strides3(v, "v"),
+                       _strides3(out, "out"))
+    b, sq, hq, d = q.shape
+    b2, sk, hkv, d2 = k.shape
+    if b2 != b or d2 != d or tuple(v.shape) != tuple(k.shape) or tuple(out.shape) != tuple(q.shape):
+        raise ValueError("inconsistent q / k / v / out shapes")
+    rc = lib.attn_fwd_dense(_ptr(out), _ptr(q), _ptr(k), _ptr(v), qs, ks, vs, os_, b, sq, sk, hq,
+                            hkv, d, float(scale), int(bool(causal)), dt, int(rounding), _ptr(lse),
+                            _ptr(status), _stream_handle(stream))
+    _check(rc, "attn_fwd_dense")
+
+
 def attn_fwd_decode(out, q, k_cache, v_cache, block_table, seq_lens, *, max_seqlen_k: int,
                     scale: float, num_splits: int, workspace=None, rounding: int = RTNE,
                     lse=None, status=None, stream=None) -> None:
@@ -274,6 +316,26 @@ def prefill(q, k_cache, v_cache, block_table, query_start_loc, seq_lens, *, max_
     attn_fwd_prefill(out, q, k_cache, v_cache, block_table, query_start_loc, seq_lens,
                      max_seqlen_q=max_seqlen_q, max_seqlen_k=max_seqlen_k, scale=scale,
                      causal=causal, rounding=rounding, lse=lse, status=status, stream=stream)
+    return (out, lse) if return_lse else out
+
+
+def dense(q, k, v, *, layout: str = "bshd", scale: float | None = None, causal: bool = False,
+          rounding: int = RTNE, return_lse: bool = False, status=None, stream=None):
+    """Returns O in the layout of q for fixed-length batches: layout "bshd"
+    takes [B, S, H, d] tensors, "bhsd" takes [B, H, S, d] tensors (read in
+    place).  The log-sum-exp, when asked, is [B, H, Sq] fp32."""
+    if layout not in ("bshd", "bhsd"):
+        raise ValueError("layout must be 'bshd' or 'bhsd'")
+    if scale is None:
+        scale = q.shape[-1] ** -0.5
+    out = torch.empty(q.shape, dtype=torch.float32 if rounding == OUT_F32 else q.dtype,
+                      device=q.device)
+    view = (lambda t: t.transpose(1, 2)) if layout == "bhsd" else (lambda t: t)
+    qv = view(q)
+    lse = (torch.empty((qv.shape[0], qv.shape[2], qv.shape[1]), dtype=torch.float32,
+                       device=q.device) if return_lse else None)
+    attn_fwd_dense(view(out), qv, view(k), view(v), scale=scale, causal=causal, rounding=rounding,
+                   lse=lse, status=status, stream=stream)
     return (out, lse) if return_lse else out
 
 

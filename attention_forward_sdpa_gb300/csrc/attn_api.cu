@@ -261,6 +261,98 @@ attn_status_t attn_fwd_prefill(void* out, const void* q, const void* k_cache, co
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
+attn_status_t attn_fwd_dense(void* out, const void* q, const void* k, const void* v,
+                             const int64_t* q_strides, const int64_t* k_strides,
+                             const int64_t* v_strides, const int64_t* o_strides, int32_t batch,
+                             int32_t seqlen_q, int32_t seqlen_k, int32_t num_q_heads,
+                             int32_t num_kv_heads, int32_t head_size, float scale, int32_t causal,
+                             attn_dtype_t dtype, attn_round_t rounding, float* lse_out,
+                             int32_t* status_dev, void* stream) {
+  // ---- host-side validation (no CUDA call before this block ends)
+  if (batch < 0 || seqlen_q < 0 || seqlen_k < 0) return ATTN_ERR_INVALID_ARG;
+  if (num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0) return ATTN_ERR_INVALID_ARG;
+  if (dtype != ATTN_F16 && dtype != ATTN_BF16) return ATTN_ERR_INVALID_ARG;
+  if (rounding < ATTN_RTNE || rounding > ATTN_OUT_F32) return ATTN_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return ATTN_ERR_INVALID_ARG;
+  if (!valid_scale(scale)) return ATTN_ERR_INVALID_ARG;
+  if (!q_strides || !k_strides || !v_strides || !o_strides) return ATTN_ERR_INVALID_ARG;
+  if (head_size != 64 && head_size != 128) return ATTN_ERR_UNSUPPORTED;
+  if (batch == 0 || seqlen_q == 0) return ATTN_OK;  // nothing to compute
+  if (!out || !q || !k || !v) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(out) || !aligned16(q) || !aligned16(k) || !aligned16(v)) return ATTN_ERR_INVALID_ARG;
+  const int64_t out_elem = rounding == ATTN_OUT_F32 ? 4 : 2;
+  for (int i = 0; i < 3; ++i) {
+    // positive strides whose byte sizes are multiples of 16 (TMA and 16-byte stores)
+    if (q_strides[i] <= 0 || k_strides[i] <= 0 || v_strides[i] <= 0 || o_strides[i] <= 0) return ATTN_ERR_INVALID_ARG;
+    if ((q_strides[i] * 2) % 16 || (k_strides[i] * 2) % 16 || (v_strides[i] * 2) % 16 ||
+        (o_strides[i] * out_elem) % 16)
+      return ATTN_ERR_INVALID_ARG;
+  }
+  const int group = num_q_heads / num_kv_heads;
+  const bool pair_heads = group % 2 == 0;
+  const int64_t row_blocks = ((int64_t)seqlen_q + 127) / 128;
+  const int64_t gz = pair_heads ? row_blocks : (row_blocks + 1) / 2;
+  const int64_t gx = pair_heads ? num_q_heads / 2 : num_q_heads;
+  if (batch > 65535 || gz > 65535) return ATTN_ERR_UNSUPPORTED;
+
+  attn_status_t st = check_device();
+  if (st != ATTN_OK) return st;
+
+  attn::PrefillParams p;
+  std::memset(&p, 0, sizeof(p));
+  const bool bf16 = dtype == ATTN_BF16;
+  const cuuint64_t d = (cuuint64_t)head_size;
+  const cuuint64_t sk_dim = (cuuint64_t)(seqlen_k > 0 ? seqlen_k : 1);   // never read when 0
+  {
+    // Q and O: dims (d, Hq, Sq, B); the tile box is 128 rows of one head
+    const cuuint64_t dims[4] = {d, (cuuint64_t)num_q_heads, (cuuint64_t)seqlen_q, (cuuint64_t)batch};
+    const cuuint32_t box[4] = {64, 1, 128, 1};
+    const cuuint64_t qs[3] = {(cuuint64_t)q_strides[2] * 2, (cuuint64_t)q_strides[1] * 2, (cuuint64_t)q_strides[0] * 2};
+    if (!attn::encode_tiled(&p.tm_q, bf16, 4, dims, qs, box, q, CU_TENSOR_MAP_SWIZZLE_128B)) return ATTN_ERR_CUDA;
+    const cuuint64_t os[3] = {(cuuint64_t)o_strides[2] * 2, (cuuint64_t)o_strides[1] * 2, (cuuint64_t)o_strides[0] * 2};
+    if (rounding != ATTN_OUT_F32 &&
+        !attn::encode_tiled(&p.tm_o, bf16, 4, dims, os, box, out, CU_TENSOR_MAP_SWIZZLE_128B))
+      return ATTN_ERR_CUDA;
+  }
+  {
+    // K and V as a paged cache whose page is the batch entry: dims (d, Hkv, Sk, B)
+    const cuuint64_t dims[4] = {d, (cuuint64_t)num_kv_heads, sk_dim, (cuuint64_t)batch};
+    const cuuint32_t box[4] = {64, 1, 128, 1};
+    const cuuint64_t ks[3] = {(cuuint64_t)k_strides[2] * 2, (cuuint64_t)k_strides[1] * 2, (cuuint64_t)k_strides[0] * 2};
+    const cuuint64_t vs[3] = {(cuuint64_t)v_strides[2] * 2, (cuuint64_t)v_strides[1] * 2, (cuuint64_t)v_strides[0] * 2};
+    if (!attn::encode_tiled(&p.tm_k, bf16, 4, dims, ks, box, k, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !attn::encode_tiled(&p.tm_v, bf16, 4, dims, vs, box, v, CU_TENSOR_MAP_SWIZZLE_128B))
+      return ATTN_ERR_CUDA;
+  }
+  p.out = out;
+  p.lse = lse_out;
+  p.status = status_dev;
+  p.num_seqs = batch;
+  p.max_seqlen_q = seqlen_q;
+  p.max_seqlen_k = seqlen_k;
+  p.total_q = (int32_t)((int64_t)batch * seqlen_q > 2147483647 ? 2147483647 : (int64_t)batch * seqlen_q);
+  p.num_q_heads = num_q_heads;
+  p.num_kv_heads = num_kv_heads;
+  // one "page" per batch entry, at least one 128-key box long
+  p.block_size = (int32_t)((sk_dim + 127) / 128 * 128);
+  p.num_blocks = batch;
+  p.box_rows = 128;
+  p.pair_heads = pair_heads ? 1 : 0;
+  p.dense = 1;
+  p.dense_sq = seqlen_q;
+  p.dense_sk = seqlen_k;
+  p.o_stride_b = o_strides[0];
+  p.o_stride_s = o_strides[1];
+  p.o_stride_h = o_strides[2];
+  p.causal = causal;
+  p.rounding = (int32_t)rounding;
+  p.scale_log2 = scale * kLog2e;
+
+  dim3 grid((unsigned)gx, (unsigned)batch, (unsigned)gz);
+  cudaError_t e = attn::launch_prefill(p, head_size, bf16, grid, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
 size_t attn_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t head_size,
                                   int32_t num_splits) {
   if (num_seqs <= 0 || num_q_heads <= 0 || head_size <= 0 || num_splits <= 0) return 0;

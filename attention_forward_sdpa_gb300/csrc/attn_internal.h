@@ -11,10 +11,11 @@ namespace attn {
 
 // One prefill launch.  Tensor maps are encoded on the host (attn_api.cu).
 struct PrefillParams {
-  CUtensorMap tm_q;   // Q  [total_q, Hq, d]: dims (d, Hq, total_q), box (64, 1, 128), 128B swizzle
+  CUtensorMap tm_q;   // Q  [total_q, Hq, d]: dims (d, Hq, total_q), box (64, 1, 128), 128B swizzle;
+                      //    dense: dims (d, Hq, Sq, B), box (64, 1, 128, 1)
   CUtensorMap tm_k;   // K  [num_blocks, bs, Hkv, d]: dims (d, Hkv, bs, num_blocks), box (64, 1, R, 1)
   CUtensorMap tm_v;   // V  same as K
-  CUtensorMap tm_o;   // O  like Q over the output (16-bit output only)
+  CUtensorMap tm_o;   // O  like Q over the output (16-bit output only): 3-D packed, 4-D dense
   void* out;          // [total_q, Hq, d] 16-bit, or fp32 when rounding == 3
   float* lse;         // [total_q, Hq] or nullptr
   int32_t* status;    // device status word or nullptr
@@ -32,6 +33,12 @@ struct PrefillParams {
   int32_t num_blocks;
   int32_t box_rows;     // rows of one K/V TMA box = min(block_size, 128)
   int32_t pair_heads;   // 1: the two Q tiles of a CTA are two heads of one group
+  int32_t dense;        // 1: fixed-length strided batch (no block table, page = batch index)
+  int32_t dense_sq;     // dense: query length of every sequence
+  int32_t dense_sk;     // dense: kv length of every sequence
+  int64_t o_stride_b;   // dense: output element strides (batch, row, head)
+  int64_t o_stride_s;
+  int64_t o_stride_h;
   int32_t causal;
   int32_t rounding;     // 0 RTNE, 1 RTNA, 2 RTZ, 3 fp32 output
   float scale_log2;     // tau * log2(e)

@@ -89,14 +89,17 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
 
   // ------------------------------------------------------------ work item
   const int b = blockIdx.y;
-  const int q_begin = p.query_start_loc[b];
-  const int q_end = p.query_start_loc[b + 1];
-  const int Sq = q_end - q_begin;
-  const int Sk = p.seq_lens[b];
-  if (q_begin < 0 || Sq < 0 || Sq > p.max_seqlen_q || q_end > p.total_q || Sk < 0 ||
-      Sk > p.max_seqlen_k) {
-    if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.z == 0) report_status(p.status, kStatusBadArg);
-    return;
+  int q_begin = 0, Sq = p.dense_sq, Sk = p.dense_sk;   // dense: rows are relative to the batch entry
+  if (!p.dense) {
+    q_begin = p.query_start_loc[b];
+    const int q_end = p.query_start_loc[b + 1];
+    Sq = q_end - q_begin;
+    Sk = p.seq_lens[b];
+    if (q_begin < 0 || Sq < 0 || Sq > p.max_seqlen_q || q_end > p.total_q || Sk < 0 ||
+        Sk > p.max_seqlen_k) {
+      if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.z == 0) report_status(p.status, kStatusBadArg);
+      return;
+    }
   }
   const int n_rb = (Sq + kBM - 1) / kBM;
   int head[2], row0[2], rows[2], n_kv[2], lim_lo[2];
@@ -170,9 +173,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         if (n_kv[t] == 0) continue;
         const uint32_t bar = bar_q_full + 8u * t;
         mbar_arrive_expect_tx(bar, L::kTileBytes);
-        for (int h = 0; h < L::kHalves; ++h)
-          tma_load_3d(sQ + t * L::kTileBytes + h * L::kHalfBytes, &p.tm_q, bar, h * 64, head[t],
-                      q_begin + row0[t]);
+        for (int h = 0; h < L::kHalves; ++h) {
+          const uint32_t dst = sQ + t * L::kTileBytes + h * L::kHalfBytes;
+          if (p.dense) tma_load_4d(dst, &p.tm_q, bar, h * 64, head[t], row0[t], b);
+          else tma_load_3d(dst, &p.tm_q, bar, h * 64, head[t], q_begin + row0[t]);
+        }
       }
       const int bs = p.block_size;
       const int n_pages = (Sk + bs - 1) / bs;
@@ -190,7 +195,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         const CUtensorMap* tm = (i & 1) ? &p.tm_v : &p.tm_k;
         const int key0 = j * kBN;
         if (bs >= kBN) {
-          int page = bt[key0 / bs];
+          const int page = p.dense ? b : bt[key0 / bs];
           if (page < 0 || page >= p.num_blocks) report_status(p.status, kStatusBadBlockTable);
           mbar_arrive_expect_tx(bar, L::kTileBytes);
           for (int h = 0; h < L::kHalves; ++h)
@@ -464,9 +469,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       named_bar_sync(1 + t, kBM);
       if (wq == 0 && lane == 0 && ok && *abort_flag == 0) {
 #pragma unroll
-        for (int h = 0; h < L::kHalves; ++h)
-          tma_store_3d(&p.tm_o, sQ + t * L::kTileBytes + h * L::kHalfBytes, h * 64, t_head,
-                       q_begin + t_row0);
+        for (int h = 0; h < L::kHalves; ++h) {
+          const uint32_t src = sQ + t * L::kTileBytes + h * L::kHalfBytes;
+          if (p.dense) tma_store_4d(&p.tm_o, src, h * 64, t_head, t_row0, b);
+          else tma_store_3d(&p.tm_o, src, h * 64, t_head, q_begin + t_row0);
+        }
         bulk_commit_group();
         bulk_wait_group_read0();
       }
@@ -476,8 +483,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       // 32 rows x 16 bytes.  Row i of the buffer holds 64 bytes of row i, its
       // four 16-byte pieces rotated by (i & 3) to spread the banks.
       uint8_t* stage = smem + L::kStageOff + (warp - 4) * 2048;
-      const int64_t row_elems = (int64_t)p.num_q_heads * D;
-      const int64_t tile_base = ((int64_t)q_begin + t_row0 + wq * 32) * row_elems + (int64_t)t_head * D;
+      // element offset of this warp's first row and the distance between rows
+      const int64_t row_elems = p.dense ? p.o_stride_s : (int64_t)p.num_q_heads * D;
+      const int64_t tile_base =
+          p.dense ? (int64_t)b * p.o_stride_b + (int64_t)(t_row0 + wq * 32) * p.o_stride_s +
+                        (int64_t)t_head * p.o_stride_h
+                  : ((int64_t)q_begin + t_row0 + wq * 32) * row_elems + (int64_t)t_head * D;
       const int rows_here = min(32, t_rows - wq * 32);   // valid rows of this warp
       auto flush = [&](int64_t col_byte) {                // write 64 bytes per row
         __syncwarp();
@@ -527,8 +538,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         }
       }
     }
-    if (ok && row_ok && p.lse)
-      p.lse[tok * p.num_q_heads + t_head] = l > 0.f ? m * kLn2 + logf(l) : -INFINITY;
+    if (ok && row_ok && p.lse) {
+      // packed: [total_q, Hq]; dense: [batch, Hq, Sq]
+      const int64_t li = p.dense ? ((int64_t)b * p.num_q_heads + t_head) * Sq + t_row0 + r
+                                 : tok * p.num_q_heads + t_head;
+      p.lse[li] = l > 0.f ? m * kLn2 + logf(l) : -INFINITY;
+    }
   }
 
   tc_fence_before();

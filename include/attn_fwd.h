@@ -102,6 +102,38 @@ attn_status_t attn_fwd_prefill(void* out, const void* q, const void* k_cache, co
                                void* stream);
 
 /*
+ * attn_fwd_dense -- the same forward for fixed-length batches held as strided
+ * tensors, with no block table: logical shapes Q, O [batch, seqlen_q,
+ * num_q_heads, head_size] and K, V [batch, seqlen_k, num_kv_heads, head_size]
+ * in any (batch, sequence, head) stride order, so that both the BSHD and the
+ * BHSD layouts of "MoonMath.ai abre un nucleo de atencion HIP para AMD MI300X
+ * ..." (7minutos.es), section "Entendiendo el nucleo", are read in place.
+ *
+ *   out, q, k, v element (b, i, h, c) lives at base + b*strides[0] + i*strides[1]
+ *                + h*strides[2] + c (c = channel, contiguous).  BSHD
+ *                [B, S, H, d]: strides {S*H*d, H*d, d}; BHSD [B, H, S, d]:
+ *                strides {H*S*d, d, S*d}.  out is dtype (fp32 for
+ *                ATTN_OUT_F32), the others dtype; base pointers 16-byte
+ *                aligned and every stride a multiple of 16 bytes.
+ *   q_strides, k_strides, v_strides, o_strides: HOST arrays of 3 int64 element
+ *                strides {batch, sequence, head}; read during the call only.
+ *   batch, seqlen_q, seqlen_k, num_q_heads, num_kv_heads, head_size (64 or 128),
+ *   scale, causal (bottom-right aligned), dtype, rounding: as for attn_fwd_prefill.
+ *   lse_out      optional [batch, num_q_heads, seqlen_q] fp32, or NULL.
+ *   status_dev, stream: as for attn_fwd_prefill.
+ * The arithmetic is that of attn_fwd_prefill on the equivalent packed and
+ * paged tensors (block_size = seqlen_k, block_table[b] = {b}); the results
+ * are bit-identical to it.
+ */
+attn_status_t attn_fwd_dense(void* out, const void* q, const void* k, const void* v,
+                             const int64_t* q_strides, const int64_t* k_strides,
+                             const int64_t* v_strides, const int64_t* o_strides, int32_t batch,
+                             int32_t seqlen_q, int32_t seqlen_k, int32_t num_q_heads,
+                             int32_t num_kv_heads, int32_t head_size, float scale, int32_t causal,
+                             attn_dtype_t dtype, attn_round_t rounding, float* lse_out,
+                             int32_t* status_dev, void* stream);
+
+/*
  * attn_decode_workspace_size -- bytes of device workspace attn_fwd_decode
  * needs for these sizes: the split partials (num_seqs * num_q_heads *
  * num_splits * (head_size + 2) fp32 values when num_splits > 1) plus 256

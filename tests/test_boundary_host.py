@@ -43,7 +43,7 @@ def declared_functions():
 
 def test_header_declares_the_entry_points():
     names = declared_functions()
-    for n in ("attn_fwd_prefill", "attn_fwd_decode", "attn_decode_workspace_size",
+    for n in ("attn_fwd_prefill", "attn_fwd_dense", "attn_fwd_decode", "attn_decode_workspace_size",
               "attn_round_f32", "attn_status_string", "attn_abi_version"):
         assert n in names
 
@@ -136,6 +136,46 @@ def decode_args(**over):
 ])
 def test_decode_rejects_bad_arguments(lib, over, code):
     assert lib.attn_fwd_decode(*decode_args(**over)) == code
+
+
+S3 = (ctypes.c_int64 * 3)
+
+
+def dense_args(**over):
+    a = dict(out=FAKE, q=FAKE, k=FAKE, v=FAKE, qs=S3(4096, 1024, 128), ks=S3(4096, 256, 128),
+             vs=S3(4096, 256, 128), os=S3(4096, 1024, 128), b=2, sq=32, sk=16, hq=8, hkv=2, d=128,
+             scale=0.088, causal=1, dtype=1, rounding=0, lse=None, status=None, stream=None)
+    a.update(over)
+    return [a[k] for k in ("out", "q", "k", "v", "qs", "ks", "vs", "os", "b", "sq", "sk", "hq",
+                           "hkv", "d", "scale", "causal", "dtype", "rounding", "lse", "status",
+                           "stream")]
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(q=None), 1),
+    (dict(out=None), 1),
+    (dict(qs=None), 1),
+    (dict(os=None), 1),
+    (dict(ks=S3(4096, 256, 0)), 1),          # zero stride
+    (dict(vs=S3(4096, -256, 128)), 1),       # negative stride
+    (dict(qs=S3(4096, 1020, 128)), 1),       # 2040 bytes: not a multiple of 16
+    (dict(os=S3(4096, 1024, 130), rounding=3), 1),
+    (dict(hq=6, hkv=4), 1),
+    (dict(d=96), 2),
+    (dict(dtype=5), 1),
+    (dict(rounding=7), 1),
+    (dict(causal=3), 1),
+    (dict(scale=-1.0), 1),
+    (dict(b=-1), 1),
+    (dict(q=ctypes.c_void_p(0x10008)), 1),
+])
+def test_dense_rejects_bad_arguments(lib, over, code):
+    assert lib.attn_fwd_dense(*dense_args(**over)) == code
+
+
+def test_dense_empty_problem_is_a_no_op(lib):
+    assert lib.attn_fwd_dense(*dense_args(b=0)) == 0
+    assert lib.attn_fwd_dense(*dense_args(sq=0)) == 0
 
 
 def test_round_rejects_bad_arguments(lib):
