@@ -69,6 +69,10 @@ def load_library() -> ctypes.CDLL:
         lib.attn_fwd_dense.restype = ctypes.c_int
         lib.attn_fwd_dense.argtypes = [P, P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, f32,
                                        i32, ctypes.c_int, ctypes.c_int, P, P, P]
+        lib.attn_test_prefill_timeout.restype = ctypes.c_int
+        lib.attn_test_prefill_timeout.argtypes = [P, P, P, P, P, i32, P, P, i32, i32, i32, i32, i32,
+                                                  i32, i32, i32, i32, f32, i32, ctypes.c_int,
+                                                  ctypes.c_int, P, ctypes.c_uint64, P]
         lib.attn_decode_workspace_size.restype = sz
         lib.attn_decode_workspace_size.argtypes = [i32, i32, i32, i32]
         lib.attn_fwd_decode.restype = ctypes.c_int

@@ -47,6 +47,8 @@ attn_status_t check_device() {
   return ATTN_OK;
 }
 
+constexpr uint64_t kDefaultWaitLimitNs = 4000000000ull;   // 4 s per pipeline wait
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 bool valid_scale(float s) { return std::isfinite(s) && s > 0.f; }
@@ -175,15 +177,18 @@ const char* attn_status_string(attn_status_t s) {
   return "unknown status";
 }
 
-attn_status_t attn_fwd_prefill(void* out, const void* q, const void* k_cache, const void* v_cache,
-                               const int32_t* block_table, int32_t block_table_stride,
-                               const int32_t* query_start_loc, const int32_t* seq_lens,
-                               int32_t num_seqs, int32_t max_seqlen_q, int32_t max_seqlen_k,
-                               int32_t total_q, int32_t num_q_heads, int32_t num_kv_heads,
-                               int32_t head_size, int32_t block_size, int32_t num_blocks,
-                               float scale, int32_t causal, attn_dtype_t dtype,
-                               attn_round_t rounding, float* lse_out, int32_t* status_dev,
-                               void* stream) {
+namespace {
+// Shared by attn_fwd_prefill and its timeout test hook: the hook passes a
+// short wait limit and asks the producer to issue nothing.
+attn_status_t prefill_impl(void* out, const void* q, const void* k_cache, const void* v_cache,
+                           const int32_t* block_table, int32_t block_table_stride,
+                           const int32_t* query_start_loc, const int32_t* seq_lens,
+                           int32_t num_seqs, int32_t max_seqlen_q, int32_t max_seqlen_k,
+                           int32_t total_q, int32_t num_q_heads, int32_t num_kv_heads,
+                           int32_t head_size, int32_t block_size, int32_t num_blocks, float scale,
+                           int32_t causal, attn_dtype_t dtype, attn_round_t rounding,
+                           float* lse_out, int32_t* status_dev, void* stream,
+                           uint64_t wait_limit_ns, int32_t stall_producer) {
   // ---- host-side validation (no CUDA call before this block ends)
   if (num_seqs < 0 || max_seqlen_q < 0 || max_seqlen_k < 0 || total_q < 0) return ATTN_ERR_INVALID_ARG;
   if (num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0) return ATTN_ERR_INVALID_ARG;
@@ -255,10 +260,46 @@ attn_status_t attn_fwd_prefill(void* out, const void* q, const void* k_cache, co
   p.causal = causal;
   p.rounding = (int32_t)rounding;
   p.scale_log2 = scale * kLog2e;
+  p.wait_limit_ns = wait_limit_ns;
+  p.stall_producer = stall_producer;
 
   dim3 grid((unsigned)gx, (unsigned)num_seqs, (unsigned)gz);
   cudaError_t e = attn::launch_prefill(p, head_size, bf16, grid, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+}  // namespace
+
+attn_status_t attn_fwd_prefill(void* out, const void* q, const void* k_cache, const void* v_cache,
+                               const int32_t* block_table, int32_t block_table_stride,
+                               const int32_t* query_start_loc, const int32_t* seq_lens,
+                               int32_t num_seqs, int32_t max_seqlen_q, int32_t max_seqlen_k,
+                               int32_t total_q, int32_t num_q_heads, int32_t num_kv_heads,
+                               int32_t head_size, int32_t block_size, int32_t num_blocks,
+                               float scale, int32_t causal, attn_dtype_t dtype,
+                               attn_round_t rounding, float* lse_out, int32_t* status_dev,
+                               void* stream) {
+  return prefill_impl(out, q, k_cache, v_cache, block_table, block_table_stride, query_start_loc,
+                      seq_lens, num_seqs, max_seqlen_q, max_seqlen_k, total_q, num_q_heads,
+                      num_kv_heads, head_size, block_size, num_blocks, scale, causal, dtype,
+                      rounding, lse_out, status_dev, stream, kDefaultWaitLimitNs, 0);
+}
+
+attn_status_t attn_test_prefill_timeout(void* out, const void* q, const void* k_cache,
+                                        const void* v_cache, const int32_t* block_table,
+                                        int32_t block_table_stride, const int32_t* query_start_loc,
+                                        const int32_t* seq_lens, int32_t num_seqs,
+                                        int32_t max_seqlen_q, int32_t max_seqlen_k,
+                                        int32_t total_q, int32_t num_q_heads,
+                                        int32_t num_kv_heads, int32_t head_size,
+                                        int32_t block_size, int32_t num_blocks, float scale,
+                                        int32_t causal, attn_dtype_t dtype, attn_round_t rounding,
+                                        int32_t* status_dev, uint64_t wait_limit_ns, void* stream) {
+  if (!status_dev) return ATTN_ERR_INVALID_ARG;
+  if (wait_limit_ns < 1000000ull || wait_limit_ns > kDefaultWaitLimitNs) return ATTN_ERR_INVALID_ARG;
+  return prefill_impl(out, q, k_cache, v_cache, block_table, block_table_stride, query_start_loc,
+                      seq_lens, num_seqs, max_seqlen_q, max_seqlen_k, total_q, num_q_heads,
+                      num_kv_heads, head_size, block_size, num_blocks, scale, causal, dtype,
+                      rounding, nullptr, status_dev, stream, wait_limit_ns, 1);
 }
 
 attn_status_t attn_fwd_dense(void* out, const void* q, const void* k, const void* v,
@@ -347,6 +388,7 @@ attn_status_t attn_fwd_dense(void* out, const void* q, const void* k, const void
   p.causal = causal;
   p.rounding = (int32_t)rounding;
   p.scale_log2 = scale * kLog2e;
+  p.wait_limit_ns = kDefaultWaitLimitNs;
 
   dim3 grid((unsigned)gx, (unsigned)batch, (unsigned)gz);
   cudaError_t e = attn::launch_prefill(p, head_size, bf16, grid, static_cast<cudaStream_t>(stream));

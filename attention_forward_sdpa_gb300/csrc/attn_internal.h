@@ -42,6 +42,8 @@ struct PrefillParams {
   int32_t causal;
   int32_t rounding;     // 0 RTNE, 1 RTNA, 2 RTZ, 3 fp32 output
   float scale_log2;     // tau * log2(e)
+  uint64_t wait_limit_ns;  // limit of every pipeline wait (the library default, or a test's)
+  int32_t stall_producer;  // test only: the producer issues no copy, so the first wait runs out
 };
 
 struct DecodeParams {

@@ -57,10 +57,10 @@ struct PrefillLayout {
 
 // Waits without regard to the abort flag: used on the way out to make sure no
 // asynchronous copy or MMA still targets this CTA's memory.
-__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
   const uint64_t t0 = global_timer_ns();
   while (!mbar_test(bar, parity)) {
-    if (global_timer_ns() - t0 > kWaitLimitNs) break;
+    if (global_timer_ns() - t0 > limit_ns) break;
   }
 }
 
@@ -168,7 +168,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
 
   if (warp == 0) {
     // ---------------------------------------------------------- producer
-    if (lane == 0) {
+    // (stall_producer: a test of the timeout path issues no copy at all, so
+    // that the first consumer wait runs out with nothing in flight)
+    if (lane == 0 && !p.stall_producer) {
       for (int t = 0; t < 2; ++t) {
         if (n_kv[t] == 0) continue;
         const uint32_t bar = bar_q_full + 8u * t;
@@ -189,7 +191,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         const int j = i >> 1;
         const int s = i % L::kStages;
         const int u = i / L::kStages;
-        if (u > 0 && !mbar_wait(bar_kv_empty + 8u * s, (u - 1) & 1, abort_flag)) break;
+        if (u > 0 && !mbar_wait(bar_kv_empty + 8u * s, (u - 1) & 1, abort_flag, p.wait_limit_ns)) break;
         const uint32_t dst = sRing + s * L::kTileBytes;
         const uint32_t bar = bar_kv_full + 8u * s;
         const CUtensorMap* tm = (i & 1) ? &p.tm_v : &p.tm_k;
@@ -215,9 +217,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       }
       // make sure no copy into this CTA's shared memory is still in flight
       for (int s = 0; s < L::kStages; ++s)
-        if (filled[s] > 0) drain_wait(bar_kv_full + 8u * s, (filled[s] - 1) & 1);
+        if (filled[s] > 0) drain_wait(bar_kv_full + 8u * s, (filled[s] - 1) & 1, p.wait_limit_ns);
       for (int t = 0; t < 2; ++t)
-        if (n_kv[t] > 0) drain_wait(bar_q_full + 8u * t, 0);
+        if (n_kv[t] > 0) drain_wait(bar_q_full + 8u * t, 0, p.wait_limit_ns);
     }
   } else if (warp == 1 && lane == 0) {
     // ---------------------------------------------------------- MMA issuer
@@ -249,10 +251,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     };
     const int nk0 = n_kv[0], nk1 = n_kv[1];
     bool ok = true;
-    if (nk0 > 0) ok = mbar_wait(bar_q_full, 0, abort_flag);
-    if (ok && nk1 > 0) ok = mbar_wait(bar_q_full + 8u, 0, abort_flag);
+    if (nk0 > 0) ok = mbar_wait(bar_q_full, 0, abort_flag, p.wait_limit_ns);
+    if (ok && nk1 > 0) ok = mbar_wait(bar_q_full + 8u, 0, abort_flag, p.wait_limit_ns);
     if (ok && n_kv_max > 0) {
-      ok = mbar_wait(bar_kv_full, 0, abort_flag);  // K_0: slot 0, first fill
+      ok = mbar_wait(bar_kv_full, 0, abort_flag, p.wait_limit_ns);  // K_0: slot 0, first fill
       if (ok) {
         tc_fence_after();
         if (nk0 > 0) {
@@ -270,7 +272,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     for (int j = 0; ok && j < n_kv_max; ++j) {
       const int iv = 2 * j + 1;                    // V_j
       const int sv = iv % L::kStages;
-      if (!mbar_wait(bar_kv_full + 8u * sv, (iv / L::kStages) & 1, abort_flag)) break;
+      if (!mbar_wait(bar_kv_full + 8u * sv, (iv / L::kStages) & 1, abort_flag, p.wait_limit_ns)) break;
       tc_fence_after();
       if ((j + 1) * kBN > Sk) {
         // keys at or past kv_len in the last tile: their V rows may hold
@@ -291,12 +293,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       const int sk = ik % L::kStages;
       const bool s0 = j + 1 < nk0, s1 = j + 1 < nk1;
       if (j < nk0) {
-        if (!mbar_wait(bar_p_full, j & 1, abort_flag)) break;
+        if (!mbar_wait(bar_p_full, j & 1, abort_flag, p.wait_limit_ns)) break;
         tc_fence_after();
         issue_pv(0, sv, j > 0);
       }
       if (s0 || s1) {
-        if (!mbar_wait(bar_kv_full + 8u * sk, (ik / L::kStages) & 1, abort_flag)) break;
+        if (!mbar_wait(bar_kv_full + 8u * sk, (ik / L::kStages) & 1, abort_flag, p.wait_limit_ns)) break;
         tc_fence_after();
       }
       if (j < nk0) {
@@ -308,7 +310,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         }
       }
       if (j < nk1) {
-        if (!mbar_wait(bar_p_full + 8u, j & 1, abort_flag)) break;
+        if (!mbar_wait(bar_p_full + 8u, j & 1, abort_flag, p.wait_limit_ns)) break;
         tc_fence_after();
         issue_pv(1, sv, j > 0);
         if (s1) {
@@ -323,7 +325,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     }
     // no MMA may still be running when TMEM is released
     umma_commit(bar_mma_done);
-    drain_wait(bar_mma_done, 0);
+    drain_wait(bar_mma_done, 0, p.wait_limit_ns);
   } else if (warp >= 4) {
     // ---------------------------------------------------------- softmax + epilogue
     const int t = (warp - 4) >> 2;
@@ -345,7 +347,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     float m = -INFINITY, l = 0.f;
     bool ok = true;
     for (int j = 0; j < t_nkv; ++j) {
-      if (!mbar_wait(bar_s_full + 8u * t, j & 1, abort_flag)) { ok = false; break; }
+      if (!mbar_wait(bar_s_full + 8u * t, j & 1, abort_flag, p.wait_limit_ns)) { ok = false; break; }
       tc_fence_after();
       uint32_t s[4][32];
 #pragma unroll
@@ -424,7 +426,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       m = m_new;
     }
     if (ok && t_nkv > 0) {
-      ok = mbar_wait(bar_o_full + 8u * t, 0, abort_flag);
+      ok = mbar_wait(bar_o_full + 8u * t, 0, abort_flag, p.wait_limit_ns);
       tc_fence_after();
     }
     const bool row_ok = r < t_rows;

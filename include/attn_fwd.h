@@ -134,6 +134,29 @@ attn_status_t attn_fwd_dense(void* out, const void* q, const void* k, const void
                              int32_t* status_dev, void* stream);
 
 /*
+ * attn_test_prefill_timeout -- TEST HOOK for the failure path, not for
+ * production use; the pages have no counterpart.  Launches attn_fwd_prefill's
+ * kernel with every pipeline wait limited to wait_limit_ns (1 ms .. 4 s;
+ * attn_fwd_prefill uses 4 s) and a producer that issues no copy, so that the
+ * first wait of every CTA runs out.  Each CTA then raises its abort flag,
+ * releases its tensor memory and records ATTN_ERR_TIMEOUT in *status_dev
+ * (required here, caller-zeroed); nothing is written to out, no copy or
+ * product is left in flight, and the device stays usable for the next call.
+ * Other arguments as attn_fwd_prefill (no lse).  Returns ATTN_OK when the
+ * launch succeeded; the timeout itself is reported through *status_dev.
+ */
+attn_status_t attn_test_prefill_timeout(void* out, const void* q, const void* k_cache,
+                                        const void* v_cache, const int32_t* block_table,
+                                        int32_t block_table_stride, const int32_t* query_start_loc,
+                                        const int32_t* seq_lens, int32_t num_seqs,
+                                        int32_t max_seqlen_q, int32_t max_seqlen_k,
+                                        int32_t total_q, int32_t num_q_heads,
+                                        int32_t num_kv_heads, int32_t head_size,
+                                        int32_t block_size, int32_t num_blocks, float scale,
+                                        int32_t causal, attn_dtype_t dtype, attn_round_t rounding,
+                                        int32_t* status_dev, uint64_t wait_limit_ns, void* stream);
+
+/*
  * attn_decode_workspace_size -- bytes of device workspace attn_fwd_decode
  * needs for these sizes: the split partials (num_seqs * num_q_heads *
  * num_splits * (head_size + 2) fp32 values when num_splits > 1) plus 256

@@ -178,6 +178,17 @@ def test_dense_empty_problem_is_a_no_op(lib):
     assert lib.attn_fwd_dense(*dense_args(sq=0)) == 0
 
 
+def test_timeout_hook_rejects_bad_arguments(lib):
+    a = prefill_args()
+    a.pop(21)   # the hook has no lse argument
+    status = ctypes.c_void_p(0x20000)
+    stream = a.pop()
+    a.pop()     # status
+    assert lib.attn_test_prefill_timeout(*a, None, 20_000_000, stream) == 1        # status required
+    assert lib.attn_test_prefill_timeout(*a, status, 999, stream) == 1             # limit < 1 ms
+    assert lib.attn_test_prefill_timeout(*a, status, 5_000_000_000, stream) == 1   # limit > 4 s
+
+
 def test_round_rejects_bad_arguments(lib):
     assert lib.attn_round_f32(FAKE, FAKE, -1, 1, 0, None) == 1
     assert lib.attn_round_f32(FAKE, FAKE, 10, 1, 3, None) == 1
