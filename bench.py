@@ -186,6 +186,15 @@ class ClockSampler:
 # the library arm
 # ----------------------------------------------------------------------------
 
+def bench_config(world: int) -> dict:
+    """The workload description both arms report."""
+    return {"workload": f"{PREFILL_WL} + {DECODE_WL}",
+            "prefill": "causal bf16 B=1 Hq=32 Hkv=8 Sq=Sk=2048 d=128 paged bs=64 permuted",
+            "decode": "bf16 B=64 Hq=32 Hkv=8 d=128 Sk~U[512,8192] paged bs=16 splits=8",
+            "l2": "flushed before every step (256 MiB write)",
+            "parallelism": f"replica x{world}" if world > 1 else "single GPU"}
+
+
 def make_problems(seed: int):
     return attn_inputs.workload(PREFILL_WL, seed=seed), attn_inputs.workload(DECODE_WL, seed=seed)
 
@@ -296,11 +305,7 @@ def run_ours(args, rank, world, dev):
         "metric": METRIC, "value": tflops, "unit": "TFLOP/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": f"{PREFILL_WL} + {DECODE_WL}",
-                   "prefill": "causal bf16 B=1 Hq=32 Hkv=8 Sq=Sk=2048 d=128 paged bs=64 permuted",
-                   "decode": "bf16 B=64 Hq=32 Hkv=8 d=128 Sk~U[512,8192] paged bs=16 splits=8",
-                   "l2": "flushed before every step (256 MiB write)",
-                   "parallelism": f"replica x{world}" if world > 1 else "single GPU"},
+        "config": bench_config(world),
         "decode": {"value": gbs, "unit": "GB/s", "frac_of_hbm": gbs / world / peaks["hbm_gbs"],
                    "bytes_per_step": dbytes, "ms_per_call": d_avg_s * 1e3},
         "prefill": {"value": tflops, "unit": "TFLOP/s",
@@ -518,8 +523,7 @@ def run_reference(args, rank, world):
         "warmup": args.warmup, "ms_per_step": wall / K * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "impl": "reference",
-        "config": {"workload": f"{PREFILL_WL} + {DECODE_WL}",
-                   "sample": f"{len(rows_p)} prefill rows + {len(rows_d)} decode rows per step"},
+        "config": bench_config(1),
         "decode": {"value": oracle_bytes(dp, rows_d) * K / td / 1e9, "unit": "GB/s"},
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
                          "sample": f"{len(rows_p)} random prefill rows + {len(rows_d)} decode "
