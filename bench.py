@@ -266,8 +266,10 @@ def run_ours(args, rank, world, dev):
 
     flops = prefill_flops(pp)
     dbytes = decode_bytes(dp)
-    tflops = world * flops * K / (p_ms_tot * 1e-3) / 1e12
-    gbs = world * dbytes * K / (d_ms_tot * 1e-3) / 1e9
+    # whole-job work: every rank's own problem (decode lengths differ by seed)
+    flops_all, dbytes_all = sum_over_ranks(world, dev, [flops, dbytes])
+    tflops = flops_all * K / (p_ms_tot * 1e-3) / 1e12
+    gbs = dbytes_all * K / (d_ms_tot * 1e-3) / 1e9
     peaks, peak_src = load_peaks()
     p_avg_s = p_ms_tot / K * 1e-3
     d_avg_s = d_ms_tot / K * 1e-3
@@ -427,10 +429,11 @@ def measure_e2e(args, pp, dp, dev, stream, attn, ws, world):
     d_ms = sum(e[1].elapsed_time(e[2]) for e in evs)
     p_ms, d_ms = max_over_ranks(world, dev, [p_ms, d_ms])
     flops = prefill_flops(pp)
-    return {"value": world * flops * n / (p_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+    flops_all, dbytes_all = sum_over_ranks(world, dev, [flops, decode_bytes(dp)])
+    return {"value": flops_all * n / (p_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
             "h2d_bytes_per_step": h2d_p + h2d_d, "d2h_bytes_per_step": d2h_p + d2h_d,
             "steps": n,
-            "decode": {"value": world * decode_bytes(dp) * n / (d_ms * 1e-3) / 1e9, "unit": "GB/s"},
+            "decode": {"value": dbytes_all * n / (d_ms * 1e-3) / 1e9, "unit": "GB/s"},
             "note": "prefill part: H2D of its inputs + kernel + D2H of O; decode part likewise"}
 
 
@@ -545,13 +548,25 @@ def barrier(world):
         dist.barrier()
 
 
-def max_over_ranks(world, dev, vals):
+def _reduce_over_ranks(world, dev, vals, op):
     if world == 1:
-        return vals
+        return list(vals)
     import torch.distributed as dist
     t = torch.tensor(vals, dtype=torch.float64, device=dev)
-    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(t, op=op)
     return t.tolist()
+
+
+def max_over_ranks(world, dev, vals):
+    """Element-wise maximum over the ranks (the slowest rank's times)."""
+    import torch.distributed as dist
+    return _reduce_over_ranks(world, dev, vals, dist.ReduceOp.MAX if world > 1 else None)
+
+
+def sum_over_ranks(world, dev, vals):
+    """Element-wise sum over the ranks (the whole job's work)."""
+    import torch.distributed as dist
+    return _reduce_over_ranks(world, dev, vals, dist.ReduceOp.SUM if world > 1 else None)
 
 
 def main():
