@@ -1,7 +1,9 @@
 // attn_api.cu -- the extern "C" boundary declared in include/attn_fwd.h:
 // argument validation (all on the host, before any launch), device check,
-// TMA descriptor encoding and grid sizing.  Every compute step runs in the
-// kernels of prefill_tcgen05.cu and decode_splitkv.cu.
+// TMA descriptor encoding and grid sizing for attn_fwd_prefill,
+// attn_fwd_dense, attn_fwd_decode and the timeout test hook.  Every compute
+// step runs in the kernels of prefill_tcgen05.cu, decode_tcgen05.cu and
+// decode_splitkv.cu.
 
 #include <cuda.h>
 #include <cuda_runtime.h>

@@ -20,9 +20,9 @@
 // Every call on a device shares the one array.  Each call first zeroes the
 // work counter at the end of its part of the array (the only value that must
 // start at zero) and then overwrites every partial o, m and l before the
-// combine reads it, so nothing of a previous call is read.  Calls that can overlap on the device -- different
-// streams without ordering between them -- race on the array and must not be
-// issued.
+// combine reads it, so nothing of a previous call is read.  Calls that can
+// overlap on the device -- different streams without ordering between them --
+// race on the array and must not be issued.
 
 #include <cuda_runtime.h>
 

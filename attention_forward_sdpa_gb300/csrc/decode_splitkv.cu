@@ -15,6 +15,13 @@
 // about one per dot product), and the softmax bookkeeping of the chunk runs on
 // GH lanes from shared memory.  The warps of a CTA keep separate states that
 // are merged in a fixed order at the end.
+//
+// This SIMT kernel serves the shapes the tcgen05 decode (decode_tcgen05.cu)
+// does not take: head size 64 and group sizes that are neither a power of two
+// up to 16 nor a multiple of 16.  The file also holds the merge kernel that
+// both split kernels use (one warp per (sequence, head): every split's (m, l)
+// in one round trip, up to eight partial rows in flight, splits merged in a
+// fixed order) and the elementwise rounding kernel behind attn_round_f32.
 
 #include <algorithm>
 

@@ -7,17 +7,26 @@
 // One CTA owns two 128-row query tiles that share one KV head: two heads of a
 // GQA group over the same rows (balanced ping-pong), or, when the group size
 // is odd, two consecutive row blocks of one head.  Warp roles:
-//   warp 0      TMA producer: Q tiles once, then K_j / V_j tiles (128 keys)
-//               into a ring of shared-memory slots (128-byte swizzle);
-//   warp 1      owns TMEM (512 columns) and issues the tcgen05 MMAs:
+//   warp 0      TMA producer (one thread): Q tiles once, then K_j / V_j tiles
+//               (128 keys) into a ring of shared-memory slots (128-byte
+//               swizzle), page by page through the block table;
+//   warp 1      owns TMEM (512 columns); one thread issues the tcgen05 MMAs:
 //               S_t = Q_t K_j^T (fp32 in TMEM), O_t += P_t V_j (P from TMEM);
 //   warps 4-7   softmax for tile 0, warps 8-11 for tile 1 (one thread per
 //               query row, tcgen05.ld of its row of S): mask, running max,
 //               exp2, running denominator, P (16-bit) written back over S,
 //               rescale of O in TMEM when the max moved, and the epilogue
-//               O / l -> RTNE / RTNA / RTZ rounding -> global store.
-// The MMA issue order S_0(j), S_1(j), PV_0(j), S_0(j+1), PV_1(j), S_1(j+1) ...
-// lets one tile's softmax overlap the other tile's matrix products.
+//               O / l -> RTNE / RTNA / RTZ rounding -> global memory (a full
+//               16-bit tile through shared memory and one TMA store, other
+//               tiles through a per-warp staging buffer).
+// The MMA issue order S_0(0), S_1(0), then per key tile PV_0(j), S_0(j+1),
+// PV_1(j), S_1(j+1) lets one tile's softmax overlap the other tile's matrix
+// products.  Every pipeline wait is bounded; one that runs out raises the
+// CTA's abort flag and the status word records ATTN_ERR_TIMEOUT.
+//
+// The same kernel serves the dense strided entry point: then the page of a
+// key tile is the batch index and Q / O are addressed by (batch, row, head)
+// strides instead of packed rows.
 //
 // TMEM map (columns): S_0 [0,128), S_1 [128,256), O_0 [256,256+d),
 // O_1 [256+d, 256+2d).  P_t overwrites the first 64 columns of S_t as packed

@@ -1,8 +1,9 @@
 // sm103_ptx.cuh -- thin inline-PTX wrappers for the sm_103a features the
-// attention kernels use: mbarriers, TMA tensor loads, tcgen05 (TMEM
-// allocation, MMA, commit, loads and stores), proxy fences and a bounded wait.
-// Each wrapper is one PTX instruction (or a short fixed sequence); the operand
-// layouts follow the PTX ISA for sm_100-family targets.
+// attention kernels use: mbarriers, TMA tensor loads and stores, tcgen05
+// (TMEM allocation, MMA, commit, loads and stores), proxy fences, packed f32x2
+// arithmetic and a bounded wait.  Each wrapper is one PTX instruction (or a
+// short fixed sequence); the operand layouts follow the PTX ISA for
+// sm_100-family targets.
 #pragma once
 
 #include <cuda.h>
@@ -10,8 +11,9 @@
 
 namespace attn {
 
-// Waits give up after this many nanoseconds of %globaltimer; a kernel then
-// records ATTN_ERR_TIMEOUT and winds down instead of hanging the device.
+// Default limit of a wait, in nanoseconds of %globaltimer (a kernel may pass
+// a shorter one); a wait that runs out makes the kernel record
+// ATTN_ERR_TIMEOUT and wind down instead of hanging the device.
 constexpr uint64_t kWaitLimitNs = 4000000000ull;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
