@@ -1,0 +1,105 @@
+"""Randomised parity sweep: seeded random paged problems over every supported
+axis -- ragged batches (including empty query ranges and zero-length KV),
+every supported block size, GQA groups odd and even, head size 64 and 128,
+fp16 and bf16, causal and non-causal, all output roundings -- each compared
+element by element with the fp64 oracle and, where asked, its log-sum-exp.
+Sizes are kept small enough for the oracle to check every row.
+
+Tolerance: the measured configurations draw inputs with sigma <= 1, where
+|O| stays below about 2 and the absolute bound 2e-2 (fp16) / 4e-2 (bf16)
+applies as it stands.  Draws with sigma = 2 give outputs up to |O| ~ 8, whose
+own 16-bit rounding (up to one unit in the last place for RTZ and RTNA:
+|O| * 2^-7 for bf16, |O| * 2^-10 for fp16) is a large part of that absolute
+bound; for them the rounding term is added to it."""
+import numpy as np
+import pytest
+import torch
+
+import attn_inputs
+from tests.helpers import TOL, as_rows, gpu_decode, gpu_prefill, max_err, oracle_run, worst
+
+pytestmark = pytest.mark.gpu
+
+PREFILL_BLOCKS = (16, 32, 64, 128, 256)
+GROUPS = ((1, 1), (2, 2), (4, 1), (4, 2), (6, 2), (8, 2), (3, 3), (16, 2), (12, 4))
+
+
+ULP_REL = {torch.bfloat16: 2.0 ** -7, torch.float16: 2.0 ** -10}
+
+
+def check(prob, got, ref, rounding):
+    if prob.meta["sigma"] <= 1.0 or rounding == 3:
+        bound = TOL[prob.dtype]
+        err = max_err(got, ref)
+    else:
+        bound = TOL[prob.dtype]
+        d = np.abs(got - ref) - np.abs(ref) * ULP_REL[prob.dtype]
+        err = float(np.max(d)) if d.size else 0.0
+        if np.isnan(got).any():
+            err = float("inf")
+    assert err <= bound, (err, worst(got, ref))
+
+
+def random_prefill(seed):
+    rng = np.random.default_rng(seed)
+    hq, hkv = GROUPS[rng.integers(len(GROUPS))]
+    d = int(rng.choice([64, 128]))
+    dtype = torch.bfloat16 if rng.random() < 0.6 else torch.float16
+    causal = bool(rng.random() < 0.7)
+    n = int(rng.integers(1, 5))
+    q_lens, kv_lens = [], []
+    for _ in range(n):
+        sq = int(rng.choice([0, 1, int(rng.integers(2, 300))]))
+        sk = int(rng.integers(0, 600))
+        if causal:
+            sk = max(sk, sq) if rng.random() < 0.8 else sk   # mostly Sk >= Sq
+        q_lens.append(sq)
+        kv_lens.append(sk)
+    if sum(q_lens) == 0:
+        q_lens[0] = 5
+    return attn_inputs.paged_problem(seed=seed, q_lens=q_lens, kv_lens=kv_lens, num_q_heads=hq,
+                                     num_kv_heads=hkv, head_size=d,
+                                     block_size=int(rng.choice(PREFILL_BLOCKS)), dtype=dtype,
+                                     causal=causal, sigma=float(rng.choice([0.5, 1.0, 2.0])),
+                                     pool_extra=int(rng.integers(0, 3)))
+
+
+@pytest.mark.parametrize("seed", range(24))
+def test_random_prefill(seed):
+    prob = random_prefill(1000 + seed)
+    rounding = seed % 4                       # RTNE, RTNA, RTZ, fp32 output
+    out, lse = gpu_prefill(prob, rounding=rounding, lse=True)
+    torch.cuda.synchronize()
+    ref, ref_lse = oracle_run(prob)
+    got = as_rows(out)
+    check(prob, got, ref, rounding)
+    g = lse.cpu().numpy().reshape(-1).astype(np.float64)
+    finite = np.isfinite(ref_lse)
+    assert np.array_equal(np.isfinite(g), finite)
+    if finite.any():
+        assert np.max(np.abs(g[finite] - ref_lse[finite])) < 2e-3
+
+
+def random_decode(seed):
+    rng = np.random.default_rng(seed)
+    hq, hkv = GROUPS[rng.integers(len(GROUPS))]
+    d = int(rng.choice([64, 128]))
+    dtype = torch.bfloat16 if rng.random() < 0.6 else torch.float16
+    n = int(rng.integers(1, 12))
+    kv_lens = [int(rng.choice([0, int(rng.integers(1, 40)), int(rng.integers(40, 3000))]))
+               for _ in range(n)]
+    return attn_inputs.paged_problem(seed=seed, q_lens=[1] * n, kv_lens=kv_lens, num_q_heads=hq,
+                                     num_kv_heads=hkv, head_size=d,
+                                     block_size=int(rng.choice([16, 32, 48, 64, 128, 256])),
+                                     dtype=dtype, causal=False,
+                                     pool_extra=int(rng.integers(0, 5)))
+
+
+@pytest.mark.parametrize("seed", range(16))
+def test_random_decode(seed):
+    prob = random_decode(2000 + seed)
+    splits = int(np.random.default_rng(seed).choice([1, 2, 3, 8, 13]))
+    out = gpu_decode(prob, splits=splits, rounding=seed % 4)
+    torch.cuda.synchronize()
+    ref, _ = oracle_run(prob)
+    check(prob, as_rows(out), ref, seed % 4)
