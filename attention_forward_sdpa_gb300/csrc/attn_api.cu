@@ -10,6 +10,7 @@
 
 #include <cmath>
 #include <cstdint>
+#include <atomic>
 #include <cstring>
 #include <mutex>
 
@@ -74,15 +75,15 @@ bool encode_tiled(CUtensorMap* map, bool bf16, int rank, const cuuint64_t* dims,
 }
 
 int device_sm_count() {
-  static int cached[64] = {};
+  static std::atomic<int> cached[64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-  if (cached[dev] == 0) {
-    int n = 0;
+  int n = cached[dev].load(std::memory_order_relaxed);
+  if (n == 0) {
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-    cached[dev] = n;
+    cached[dev].store(n, std::memory_order_relaxed);
   }
-  return cached[dev];
+  return n;
 }
 
 // Workspace: [partial o: rows * splits * d fp32][partial (m, l): rows * splits

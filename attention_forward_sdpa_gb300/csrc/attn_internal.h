@@ -2,6 +2,7 @@
 // kernel launchers (not part of the public interface).
 #pragma once
 
+#include <atomic>
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cstddef>
@@ -97,6 +98,22 @@ bool encode_tiled(CUtensorMap* map, bool bf16, int rank, const cuuint64_t* dims,
                   const cuuint64_t* strides_bytes, const cuuint32_t* box, const void* base,
                   CUtensorMapSwizzle swz);
 int device_sm_count();
+
+// Opts `kernel` in to `bytes` of dynamic shared memory on the current device.
+// Function attributes are per device, so `done` (one per kernel) records the
+// devices already set up; setting an attribute twice is harmless, so two
+// threads racing here only repeat the call.
+template <typename Kernel>
+cudaError_t ensure_dynamic_smem(Kernel kernel, int bytes, std::atomic<uint64_t>& done) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = dev >= 0 && dev < 64 ? (1ull << dev) : 0ull;
+  if (bit != 0 && (done.load(std::memory_order_acquire) & bit) != 0) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && bit != 0) done.fetch_or(bit, std::memory_order_release);
+  return e;
+}
 
 cudaError_t launch_round(void* out, const float* in, int64_t n, bool bf16, int mode,
                          cudaStream_t stream);

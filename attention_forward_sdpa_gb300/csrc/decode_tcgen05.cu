@@ -626,13 +626,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
 
 template <bool BF16, int GH>
 cudaError_t launch_t(const DecodeParams& p, int grid, cudaStream_t stream) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<BF16, GH>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static std::atomic<uint64_t> smem_set{0};
+  const cudaError_t e = ensure_dynamic_smem(decode_tc_kernel<BF16, GH>, kSmemBytes, smem_set);
+  if (e != cudaSuccess) return e;
   decode_tc_kernel<BF16, GH><<<grid, kThreads, kSmemBytes, stream>>>(p);
   return cudaGetLastError();
 }

@@ -569,13 +569,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
 template <int D, bool BF16>
 cudaError_t launch_one(const PrefillParams& p, dim3 grid, cudaStream_t stream) {
   using L = PrefillLayout<D>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(prefill_kernel<D, BF16>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static std::atomic<uint64_t> smem_set{0};
+  const cudaError_t e = ensure_dynamic_smem(prefill_kernel<D, BF16>, L::kSmemBytes, smem_set);
+  if (e != cudaSuccess) return e;
   prefill_kernel<D, BF16><<<grid, kThreads, L::kSmemBytes, stream>>>(p);
   return cudaGetLastError();
 }
