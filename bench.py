@@ -61,8 +61,8 @@ CSRC = os.path.join(ROOT, "attention_forward_sdpa_gb300", "csrc")
 # edit of comments alone keeps it; the ncu summaries under profiles/ record
 # each capture).
 MEASURED_TRAFFIC = {
-    "prefill": ("prefill_tcgen05.cu", "0daba268ff01bc57", 25.241088e6 + 768.0),
-    "decode": ("decode_tcgen05.cu", "bd111ed0860b54d1", 1.130829e9 + 9.364224e6),
+    "prefill": ("prefill_tcgen05.cu", "b7b90a6bcd729b89", 25.241088e6 + 512.0),
+    "decode": ("decode_tcgen05.cu", "6d3a0c8a3e4abc34", 1.130830e9 + 9.613056e6),
 }
 
 
