@@ -58,6 +58,21 @@ bool valid_scale(float s) { return std::isfinite(s) && s > 0.f; }
 
 constexpr float kLog2e = 1.4426950408889634f;
 
+// Prefill grid (x: head units, z: row units; y is the sequence).  Head sizes
+// 64 and 128 put two 128-row query tiles in a CTA: two heads of a GQA group
+// when the group size is even, else two row blocks of one head.  Head size
+// 256 has one query tile per CTA.
+void prefill_grid(int head_size, bool pair_heads, int num_q_heads, int64_t row_blocks, int64_t& gx,
+                  int64_t& gz) {
+  if (head_size == 256) {
+    gx = num_q_heads;
+    gz = row_blocks;
+  } else {
+    gx = pair_heads ? num_q_heads / 2 : num_q_heads;
+    gz = pair_heads ? row_blocks : (row_blocks + 1) / 2;
+  }
+}
+
 }  // namespace
 
 namespace attn {
@@ -200,7 +215,7 @@ attn_status_t prefill_impl(void* out, const void* q, const void* k_cache, const 
   if (causal != 0 && causal != 1) return ATTN_ERR_INVALID_ARG;
   if (!valid_scale(scale)) return ATTN_ERR_INVALID_ARG;
   if (block_size <= 0 || num_blocks <= 0) return ATTN_ERR_INVALID_ARG;
-  if (head_size != 64 && head_size != 128) return ATTN_ERR_UNSUPPORTED;
+  if (head_size != 64 && head_size != 128 && head_size != 256) return ATTN_ERR_UNSUPPORTED;
   if (block_size % 16 != 0 || !(128 % block_size == 0 || block_size % 128 == 0)) return ATTN_ERR_UNSUPPORTED;
   if (num_seqs == 0 || total_q == 0 || max_seqlen_q == 0) return ATTN_OK;  // nothing to compute
   if (!out || !q || !k_cache || !v_cache || !block_table || !query_start_loc || !seq_lens)
@@ -212,8 +227,8 @@ attn_status_t prefill_impl(void* out, const void* q, const void* k_cache, const 
   const int group = num_q_heads / num_kv_heads;
   const bool pair_heads = group % 2 == 0;
   const int64_t row_blocks = ((int64_t)max_seqlen_q + 127) / 128;
-  const int64_t gz = pair_heads ? row_blocks : (row_blocks + 1) / 2;
-  const int64_t gx = pair_heads ? num_q_heads / 2 : num_q_heads;
+  int64_t gz = 0, gx = 0;
+  prefill_grid(head_size, pair_heads, num_q_heads, row_blocks, gx, gz);
   if (num_seqs > 65535 || gz > 65535 || gx > 2147483647) return ATTN_ERR_UNSUPPORTED;
 
   attn_status_t st = check_device();
@@ -239,8 +254,10 @@ attn_status_t prefill_impl(void* out, const void* q, const void* k_cache, const 
     const cuuint64_t strides[3] = {d * 2, d * 2 * (cuuint64_t)num_kv_heads,
                                    d * 2 * (cuuint64_t)num_kv_heads * (cuuint64_t)block_size};
     const cuuint32_t box[4] = {64, 1, (cuuint32_t)(block_size < 128 ? block_size : 128), 1};
+    // head size 256 reads V in 64-key halves of a key tile
+    const cuuint32_t vbox[4] = {64, 1, (cuuint32_t)(head_size == 256 && block_size > 64 ? 64 : box[2]), 1};
     if (!attn::encode_tiled(&p.tm_k, bf16, 4, dims, strides, box, k_cache, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !attn::encode_tiled(&p.tm_v, bf16, 4, dims, strides, box, v_cache, CU_TENSOR_MAP_SWIZZLE_128B))
+        !attn::encode_tiled(&p.tm_v, bf16, 4, dims, strides, vbox, v_cache, CU_TENSOR_MAP_SWIZZLE_128B))
       return ATTN_ERR_CUDA;
   }
   p.out = out;
@@ -320,7 +337,7 @@ attn_status_t attn_fwd_dense(void* out, const void* q, const void* k, const void
   if (causal != 0 && causal != 1) return ATTN_ERR_INVALID_ARG;
   if (!valid_scale(scale)) return ATTN_ERR_INVALID_ARG;
   if (!q_strides || !k_strides || !v_strides || !o_strides) return ATTN_ERR_INVALID_ARG;
-  if (head_size != 64 && head_size != 128) return ATTN_ERR_UNSUPPORTED;
+  if (head_size != 64 && head_size != 128 && head_size != 256) return ATTN_ERR_UNSUPPORTED;
   if (batch == 0 || seqlen_q == 0) return ATTN_OK;  // nothing to compute
   if (!out || !q || !k || !v) return ATTN_ERR_INVALID_ARG;
   if (!aligned16(out) || !aligned16(q) || !aligned16(k) || !aligned16(v)) return ATTN_ERR_INVALID_ARG;
@@ -335,8 +352,8 @@ attn_status_t attn_fwd_dense(void* out, const void* q, const void* k, const void
   const int group = num_q_heads / num_kv_heads;
   const bool pair_heads = group % 2 == 0;
   const int64_t row_blocks = ((int64_t)seqlen_q + 127) / 128;
-  const int64_t gz = pair_heads ? row_blocks : (row_blocks + 1) / 2;
-  const int64_t gx = pair_heads ? num_q_heads / 2 : num_q_heads;
+  int64_t gz = 0, gx = 0;
+  prefill_grid(head_size, pair_heads, num_q_heads, row_blocks, gx, gz);
   if (batch > 65535 || gz > 65535) return ATTN_ERR_UNSUPPORTED;
 
   attn_status_t st = check_device();
@@ -362,10 +379,11 @@ attn_status_t attn_fwd_dense(void* out, const void* q, const void* k, const void
     // K and V as a paged cache whose page is the batch entry: dims (d, Hkv, Sk, B)
     const cuuint64_t dims[4] = {d, (cuuint64_t)num_kv_heads, sk_dim, (cuuint64_t)batch};
     const cuuint32_t box[4] = {64, 1, 128, 1};
+    const cuuint32_t vbox[4] = {64, 1, head_size == 256 ? 64u : 128u, 1};
     const cuuint64_t ks[3] = {(cuuint64_t)k_strides[2] * 2, (cuuint64_t)k_strides[1] * 2, (cuuint64_t)k_strides[0] * 2};
     const cuuint64_t vs[3] = {(cuuint64_t)v_strides[2] * 2, (cuuint64_t)v_strides[1] * 2, (cuuint64_t)v_strides[0] * 2};
     if (!attn::encode_tiled(&p.tm_k, bf16, 4, dims, ks, box, k, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !attn::encode_tiled(&p.tm_v, bf16, 4, dims, vs, box, v, CU_TENSOR_MAP_SWIZZLE_128B))
+        !attn::encode_tiled(&p.tm_v, bf16, 4, dims, vs, vbox, v, CU_TENSOR_MAP_SWIZZLE_128B))
       return ATTN_ERR_CUDA;
   }
   p.out = out;
@@ -422,7 +440,7 @@ attn_status_t attn_fwd_decode(void* out, const void* q, const void* k_cache, con
   if (!valid_scale(scale)) return ATTN_ERR_INVALID_ARG;
   if (block_size <= 0 || num_blocks <= 0) return ATTN_ERR_INVALID_ARG;
   if (num_splits < 1 || num_splits > 64) return ATTN_ERR_INVALID_ARG;
-  if (head_size != 64 && head_size != 128) return ATTN_ERR_UNSUPPORTED;
+  if (head_size != 64 && head_size != 128 && head_size != 256) return ATTN_ERR_UNSUPPORTED;
   if (block_size % 16 != 0) return ATTN_ERR_UNSUPPORTED;
   if (num_seqs == 0) return ATTN_OK;
   if (!out || !q || !k_cache || !v_cache || !block_table || !seq_lens) return ATTN_ERR_INVALID_ARG;

@@ -15,7 +15,7 @@ struct PrefillParams {
   CUtensorMap tm_q;   // Q  [total_q, Hq, d]: dims (d, Hq, total_q), box (64, 1, 128), 128B swizzle;
                       //    dense: dims (d, Hq, Sq, B), box (64, 1, 128, 1)
   CUtensorMap tm_k;   // K  [num_blocks, bs, Hkv, d]: dims (d, Hkv, bs, num_blocks), box (64, 1, R, 1)
-  CUtensorMap tm_v;   // V  same as K
+  CUtensorMap tm_v;   // V  same as K; head size 256: box rows min(block_size, 64)
   CUtensorMap tm_o;   // O  like Q over the output (16-bit output only): 3-D packed, 4-D dense
   void* out;          // [total_q, Hq, d] 16-bit, or fp32 when rounding == 3
   float* lse;         // [total_q, Hq] or nullptr
@@ -81,6 +81,7 @@ struct DecodeParams {
 // Launchers return a cudaError_t from the launch.
 cudaError_t launch_prefill(const PrefillParams& p, int head_size, bool bf16, dim3 grid,
                            cudaStream_t stream);
+cudaError_t launch_prefill_d256(const PrefillParams& p, bool bf16, dim3 grid, cudaStream_t stream);
 cudaError_t launch_decode(const DecodeParams& p, int head_size, bool bf16, int group,
                           cudaStream_t stream);
 cudaError_t launch_decode_tc(const DecodeParams& p, bool bf16, int grid, cudaStream_t stream);

@@ -77,7 +77,7 @@ extern "C" attn_status_t attn_fwd_decode_noalloc(
   if (!std::isfinite(scale) || !(scale > 0.f)) return ATTN_ERR_INVALID_ARG;
   if (block_size <= 0 || num_blocks <= 0) return ATTN_ERR_INVALID_ARG;
   if (num_splits < 1 || num_splits > 64) return ATTN_ERR_INVALID_ARG;
-  if (head_size != 64 && head_size != 128) return ATTN_ERR_UNSUPPORTED;
+  if (head_size != 64 && head_size != 128 && head_size != 256) return ATTN_ERR_UNSUPPORTED;
   if (block_size % 16 != 0) return ATTN_ERR_UNSUPPORTED;
   if (num_seqs == 0) return ATTN_OK;
   if (!out || !q || !k_cache || !v_cache || !block_table || !seq_lens) return ATTN_ERR_INVALID_ARG;

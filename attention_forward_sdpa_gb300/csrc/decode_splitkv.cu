@@ -67,9 +67,27 @@ __device__ __forceinline__ int scatter_index(int lane, int k) {
   else return lane / (32 / N);
 }
 
+template <bool BF16>
+__device__ __forceinline__ void widen2(uint32_t w, float& lo, float& hi) {
+  if constexpr (BF16) {
+    lo = __uint_as_float(w << 16);
+    hi = __uint_as_float(w & 0xFFFF0000u);
+  } else {
+    const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&w));
+    lo = a.x;
+    hi = a.y;
+  }
+}
+
 template <bool BF16, int DPL>
 __device__ __forceinline__ void load_row(const uint16_t* __restrict__ src, float (&x)[DPL]) {
-  if constexpr (DPL == 4) {
+  if constexpr (DPL == 8) {
+    const uint4 w = __ldg(reinterpret_cast<const uint4*>(src));
+    widen2<BF16>(w.x, x[0], x[1]);
+    widen2<BF16>(w.y, x[2], x[3]);
+    widen2<BF16>(w.z, x[4], x[5]);
+    widen2<BF16>(w.w, x[6], x[7]);
+  } else if constexpr (DPL == 4) {
     const uint2 w = __ldg(reinterpret_cast<const uint2*>(src));
     if constexpr (BF16) {
       x[0] = __uint_as_float(w.x << 16);
@@ -116,7 +134,7 @@ __device__ __forceinline__ void store_out(void* out, int64_t idx, const float* v
 template <int D, bool BF16, int GH>
 __global__ void __launch_bounds__(kDecWarps * 32) decode_split_kernel(const __grid_constant__ DecodeParams p) {
   constexpr int DPL = D / 32;             // channels per lane
-  constexpr int CK = GH <= 4 ? 16 : 8;    // keys per chunk
+  constexpr int CK = (GH <= 4 && D <= 128) ? 16 : 8;    // keys per chunk
   constexpr int N = CK * GH;              // dot products per chunk
   constexpr int NV = N >= 32 ? N / 32 : 1;
 
@@ -298,7 +316,7 @@ __global__ void __launch_bounds__(kDecWarps * 32) decode_split_kernel(const __gr
 // units), summed in split order.  One warp per (sequence, q head).
 template <int D, bool BF16>
 __global__ void __launch_bounds__(128) decode_combine_kernel(const __grid_constant__ DecodeParams p) {
-  constexpr int DPL = D / 32;                   // channels per lane: 4 at d = 128, 2 at d = 64
+  constexpr int DPL = D / 32;                   // channels per lane: 8, 4 or 2 at d = 256, 128, 64
   const int lane = threadIdx.x & 31;
   const int64_t row = (int64_t)blockIdx.x * 4 + (threadIdx.x >> 5);
   if (row >= (int64_t)p.num_seqs * p.num_q_heads) return;
@@ -341,9 +359,12 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(const __grid_consta
       const float w = __shfl_sync(0xFFFFFFFFu, sp < 32 ? w_a : w_b, sp & 31);
       wg[u] = sp < S ? w : 0.f;
       if (sp < S) {
-        if constexpr (DPL == 4) {
-          const float4 x = *reinterpret_cast<const float4*>(po + (int64_t)sp * D);
-          v[u][0] = x.x; v[u][1] = x.y; v[u][2] = x.z; v[u][3] = x.w;
+        if constexpr (DPL % 4 == 0) {
+#pragma unroll
+          for (int q4 = 0; q4 < DPL / 4; ++q4) {
+            const float4 x = *reinterpret_cast<const float4*>(po + (int64_t)sp * D + 4 * q4);
+            v[u][4 * q4] = x.x; v[u][4 * q4 + 1] = x.y; v[u][4 * q4 + 2] = x.z; v[u][4 * q4 + 3] = x.w;
+          }
         } else {
           const float2 x = *reinterpret_cast<const float2*>(po + (int64_t)sp * D);
           v[u][0] = x.x; v[u][1] = x.y;
@@ -388,7 +409,9 @@ cudaError_t launch_decode_d(const DecodeParams& p, int gh, cudaStream_t stream) 
     case 1: return launch_decode_t<D, BF16, 1>(p, stream);
     case 2: return launch_decode_t<D, BF16, 2>(p, stream);
     case 4: return launch_decode_t<D, BF16, 4>(p, stream);
-    case 8: return launch_decode_t<D, BF16, 8>(p, stream);
+    case 8:
+      if constexpr (D <= 128) return launch_decode_t<D, BF16, 8>(p, stream);
+      else return cudaErrorInvalidValue;
     default: return cudaErrorInvalidValue;
   }
 }
@@ -403,16 +426,19 @@ __global__ void round_kernel(void* out, const float* in, int64_t n, int bf16, in
 
 }  // namespace
 
-// Heads handled per CTA: the largest of 8, 4, 2, 1 that divides the group.
-static int heads_per_cta(int group) {
-  for (int gh = 8; gh > 1; gh >>= 1)
+// Heads handled per CTA: the largest of 8, 4, 2, 1 that divides the group
+// (at most 4 at head size 256, whose per-warp partial rows would otherwise
+// exceed the static shared memory of a CTA).
+static int heads_per_cta(int group, int head_size) {
+  for (int gh = head_size == 256 ? 4 : 8; gh > 1; gh >>= 1)
     if (group % gh == 0) return gh;
   return 1;
 }
 
 cudaError_t launch_decode(const DecodeParams& p, int head_size, bool bf16, int group,
                           cudaStream_t stream) {
-  const int gh = heads_per_cta(group);
+  const int gh = heads_per_cta(group, head_size);
+  if (head_size == 256) return bf16 ? launch_decode_d<256, true>(p, gh, stream) : launch_decode_d<256, false>(p, gh, stream);
   if (head_size == 128) return bf16 ? launch_decode_d<128, true>(p, gh, stream) : launch_decode_d<128, false>(p, gh, stream);
   if (head_size == 64) return bf16 ? launch_decode_d<64, true>(p, gh, stream) : launch_decode_d<64, false>(p, gh, stream);
   return cudaErrorInvalidValue;
@@ -420,6 +446,7 @@ cudaError_t launch_decode(const DecodeParams& p, int head_size, bool bf16, int g
 
 cudaError_t launch_decode_combine(const DecodeParams& p, int head_size, bool bf16,
                                   cudaStream_t stream) {
+  if (head_size == 256) return bf16 ? launch_combine_t<256, true>(p, stream) : launch_combine_t<256, false>(p, stream);
   if (head_size == 128) return bf16 ? launch_combine_t<128, true>(p, stream) : launch_combine_t<128, false>(p, stream);
   if (head_size == 64) return bf16 ? launch_combine_t<64, true>(p, stream) : launch_combine_t<64, false>(p, stream);
   return cudaErrorInvalidValue;

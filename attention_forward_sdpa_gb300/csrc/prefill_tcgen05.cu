@@ -582,6 +582,7 @@ cudaError_t launch_prefill(const PrefillParams& p, int head_size, bool bf16, dim
                            cudaStream_t stream) {
   if (head_size == 128) return bf16 ? launch_one<128, true>(p, grid, stream) : launch_one<128, false>(p, grid, stream);
   if (head_size == 64) return bf16 ? launch_one<64, true>(p, grid, stream) : launch_one<64, false>(p, grid, stream);
+  if (head_size == 256) return launch_prefill_d256(p, bf16, grid, stream);
   return cudaErrorInvalidValue;
 }
 

@@ -24,6 +24,9 @@ Reported (one JSON line on rank 0):
   cpu_baseline the fp64 CPU oracle on a bounded row sample of the same
                workloads (rank 0, single-GPU runs only).
 `--impl reference` times the oracle instead (the reference arm).
+`--sweep` times every named workload on its own instead (one JSON line each:
+one call per timed iteration, L2 flushed before each, median of CUDA-event
+times, clocks sampled meanwhile); these lines are not the benchmark line.
 Multi-GPU: every rank runs its own copy of the workload (independent
 problems, no collective on the data path); value is the sum over ranks of the
 work divided by the slowest rank's time (weak scaling).
@@ -549,6 +552,69 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+def run_sweep(args, dev):
+    """One line per named workload (see --sweep)."""
+    import attention_forward_sdpa_gb300 as attn
+
+    attn.load_library()
+    peaks, peak_src = load_peaks()
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    names = args.sweep.split(",") if args.sweep != "all" else list(attn_inputs.WORKLOADS)
+    for name in names:
+        prob = attn_inputs.workload(name)
+        t = device_args(prob, dev)
+        out = torch.empty_like(t["q"])
+        is_decode = prob.max_seqlen_q == 1
+        if is_decode:
+            ws = torch.empty(attn.attn_decode_workspace_size(prob.num_seqs, prob.num_q_heads,
+                                                             prob.head_size, DECODE_SPLITS),
+                             dtype=torch.uint8, device=dev)
+
+            def call():
+                attn.attn_fwd_decode(out, t["q"], t["k_cache"], t["v_cache"], t["block_table"],
+                                     t["seq_lens"], max_seqlen_k=prob.max_seqlen_k,
+                                     scale=prob.scale, num_splits=DECODE_SPLITS, workspace=ws,
+                                     stream=stream)
+        else:
+            def call():
+                attn.attn_fwd_prefill(out, t["q"], t["k_cache"], t["v_cache"], t["block_table"],
+                                      t["query_start_loc"], t["seq_lens"],
+                                      max_seqlen_q=prob.max_seqlen_q,
+                                      max_seqlen_k=prob.max_seqlen_k, scale=prob.scale,
+                                      causal=prob.causal, stream=stream)
+        for _ in range(args.warmup):
+            flush.zero_()
+            call()
+        torch.cuda.synchronize(dev)
+        n = 5 if prob.total_q * prob.num_q_heads > (1 << 22) else 20
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(n)]
+        sampler = ClockSampler(dev.index if dev.index is not None else 0)
+        sampler.start()
+        time.sleep(0.3)
+        t0 = time.time()
+        for a, b in evs:
+            flush.zero_()
+            a.record(stream)
+            call()
+            b.record(stream)
+        torch.cuda.synchronize(dev)
+        t1 = time.time()
+        time.sleep(0.1)
+        sampler.stop()
+        us = statistics.median(a.elapsed_time(b) for a, b in evs) * 1e3
+        if is_decode:
+            value, unit, peak = decode_bytes(prob) / us / 1e3, "GB/s", peaks["hbm_gbs"]
+        else:
+            value, unit, peak = prefill_flops(prob) / us / 1e6, "TFLOP/s", peaks["bf16_tflops"]
+        print(json.dumps({"workload": name, "us": us, "value": value, "unit": unit,
+                          "frac": value / peak, "peak": peak, "peak_source": peak_src,
+                          "calls": n, "clocks": sampler.summary(t0, t1)}), flush=True)
+        del t, out
+        torch.cuda.empty_cache()
+
+
 # ----------------------------------------------------------------------------
 # distributed plumbing
 # ----------------------------------------------------------------------------
@@ -592,6 +658,8 @@ def main():
     ap.add_argument("--no-graph", action="store_true", help="skip the CUDA-graph replay timings")
     ap.add_argument("--cpu-seconds", type=float, default=16.0)
     ap.add_argument("--ref-rows", type=int, default=128)
+    ap.add_argument("--sweep", nargs="?", const="all", default=None,
+                    help="time each named workload (comma-separated names, default all)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -604,6 +672,10 @@ def main():
         return
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
+    if args.sweep:
+        if rank == 0:
+            run_sweep(args, dev)
+        return
     if world > 1:
         import torch.distributed as dist
         os.environ.setdefault("MASTER_ADDR", "127.0.0.1")

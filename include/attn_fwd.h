@@ -80,7 +80,9 @@ typedef enum { ATTN_RTNE = 0, ATTN_RTNA = 1, ATTN_RTZ = 2, ATTN_OUT_F32 = 3 } at
  *   seq_lens     [num_seqs] int32: kv length of each sequence.
  *   max_seqlen_q / max_seqlen_k: upper bounds of the per-sequence lengths
  *                (used to size the grid; violations are reported on the device).
- *   head_size    64 or 128.  block_size: a multiple of 16 that divides 128,
+ *   head_size    64, 128 or 256 (the pages leave 256 without a tiled kernel,
+ *                "gfx942 unified attention -- parity + benchmark harness",
+ *                Troubleshooting; here it has one).  block_size: a multiple of 16 that divides 128,
  *                or a multiple of 128.  num_q_heads % num_kv_heads == 0.
  *   scale        tau (> 0), normally 1/sqrt(head_size).
  *   causal       0 or 1 (bottom-right aligned).
@@ -117,7 +119,7 @@ attn_status_t attn_fwd_prefill(void* out, const void* q, const void* k_cache, co
  *                aligned and every stride a multiple of 16 bytes.
  *   q_strides, k_strides, v_strides, o_strides: HOST arrays of 3 int64 element
  *                strides {batch, sequence, head}; read during the call only.
- *   batch, seqlen_q, seqlen_k, num_q_heads, num_kv_heads, head_size (64 or 128),
+ *   batch, seqlen_q, seqlen_k, num_q_heads, num_kv_heads, head_size (64, 128 or 256),
  *   scale, causal (bottom-right aligned), dtype, rounding: as for attn_fwd_prefill.
  *   lse_out      optional [batch, num_q_heads, seqlen_q] fp32, or NULL.
  *   status_dev, stream: as for attn_fwd_prefill.

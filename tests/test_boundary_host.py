@@ -87,7 +87,8 @@ def prefill_args(**over):
     (dict(hq=6, hkv=4), 1),
     (dict(hkv=0), 1),
     (dict(d=96), 2),
-    (dict(d=256), 2),
+    (dict(d=512), 2),
+    (dict(d=32), 2),
     (dict(bs=48), 2),
     (dict(bs=8), 2),
     (dict(bs=192), 2),
