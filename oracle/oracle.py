@@ -57,6 +57,10 @@ def _load():
         lib.oracle_sdpa_run.restype = ctypes.c_int
         lib.oracle_sdpa_run.argtypes = [P, P, P, P, P, P, i32, P, P, i32, i32, i32,
                                         i32, i32, f64, i32, i32, i32, i32, P, i64, i32]
+        lib.oracle_sdpa_run_ex.restype = ctypes.c_int
+        lib.oracle_sdpa_run_ex.argtypes = [P, P, P, P, P, P, i32, P, P, i32, i32, i32,
+                                           i32, i32, f64, i32, i32, i32, i32, P, i64, i32,
+                                           i32, i32, f64, P, P]
         lib.oracle_round_f32.restype = None
         lib.oracle_round_f32.argtypes = [P, P, i64, i32, i32]
         lib.oracle_widen16_array.restype = None
@@ -92,7 +96,8 @@ def default_threads() -> int:
 def sdpa(q, k_cache, v_cache, block_table, query_start_loc, seq_lens, *,
          num_q_heads: int, num_kv_heads: int, head_size: int, block_size: int,
          scale: float, causal: bool, dtype: int, rows=None, variant: int = 0,
-         param: int = 0, n_threads: int | None = None, want_lse: bool = True):
+         param: int = 0, n_threads: int | None = None, want_lse: bool = True,
+         window=(-1, -1), softcap: float = 0.0, alibi_slopes=None, sinks=None):
     """fp64 SDPA over the paged problem.
 
     Returns (out, lse): out is float64 [n_rows, head_size] with rows in
@@ -103,6 +108,12 @@ def sdpa(q, k_cache, v_cache, block_table, query_start_loc, seq_lens, *,
     variant 0 = definition ([ALG] sec. 1, 2, 4, 5, 10); 1 = online recurrence
     with tile width ``param`` ([ALG] sec. 3); 2 = ``param``-way split with a
     log-sum-exp combine ([ALG] sec. 8).
+
+    Feature flags (variant 0 only; named in [ALG] sec. 9, defined in
+    sdpa_oracle.c): ``window`` = (left, right) sliding window around the
+    aligned key (-1 = unbounded), ``softcap`` > 0 caps the scaled score at
+    c * tanh(s / c), ``alibi_slopes`` [Hq] adds -a_h * |diag - j|, ``sinks``
+    [Hq] adds e^(z_h) to the softmax denominator.
     """
     lib = _load()
     qa, ka, va = _u16(q), _u16(k_cache), _u16(v_cache)
@@ -120,13 +131,26 @@ def sdpa(q, k_cache, v_cache, block_table, query_start_loc, seq_lens, *,
         n_rows = int(rows_a.shape[0])
     out = np.zeros((n_rows, head_size), dtype=np.float64)
     lse = np.zeros((n_rows,), dtype=np.float64) if want_lse else None
-    rc = lib.oracle_sdpa_run(
+
+    def per_head(x):
+        if x is None:
+            return None
+        if not isinstance(x, np.ndarray):
+            x = x.detach().cpu().numpy() if hasattr(x, "detach") else np.asarray(x)
+        a = np.ascontiguousarray(x, dtype=np.float64).reshape(-1)
+        if a.shape[0] != num_q_heads:
+            raise ValueError("per-head feature arrays need num_q_heads entries")
+        return a
+
+    al, sk = per_head(alibi_slopes), per_head(sinks)
+    rc = lib.oracle_sdpa_run_ex(
         _ptr(out), _ptr(lse) if lse is not None else None,
         _ptr(qa), _ptr(ka), _ptr(va), _ptr(bt), int(bt.shape[1]), _ptr(qsl), _ptr(sl),
         num_seqs, num_q_heads, num_kv_heads, head_size, block_size,
         float(scale), int(bool(causal)), int(dtype), int(variant), int(param),
         _ptr(rows_a) if rows_a is not None else None, n_rows,
-        int(n_threads or default_threads()))
+        int(n_threads or default_threads()), int(window[0]), int(window[1]), float(softcap),
+        _ptr(al) if al is not None else None, _ptr(sk) if sk is not None else None)
     if rc != 0:
         raise ValueError("oracle rejected the problem description")
     return out, lse

@@ -37,9 +37,23 @@
  *   oracle_widen16           -- exact widening of bf16 / fp16 bit patterns to
  *                               binary64, from the formats' definitions.
  *
+ * Feature-flagged variants (variant 0 only).  [ALG] sec. 9 names sinks,
+ * ALiBi, softcap, sliding window (and fp8) as flags the dispatcher keeps out
+ * of graph replay, without defining them; the oracle takes their usual
+ * definitions, with diag = i + (kv_len - query_len) the key aligned with
+ * query row i:
+ *   sliding window (left W_l, right W_r; -1 = unbounded): key j is visible
+ *       only if diag - W_l <= j <= diag + W_r (on top of j < kv_len and, when
+ *       causal, j <= diag);
+ *   softcap c > 0: the scaled score s = tau q.k becomes c * tanh(s / c);
+ *   ALiBi slope a_h: the score gains -a_h * |diag - j| (after the softcap);
+ *   sink z_h: one more logit in the softmax denominator with no value row,
+ *       O = sum_j e^(s_j) V_j / (sum_j e^(s_j) + e^(z_h)); the log-sum-exp
+ *       includes it.
+ *
  * Readings where the pages are silent:
  *   - A query row with no visible key (causal with query_len > kv_len, or
- *     kv_len == 0) has output 0 and log-sum-exp -inf.
+ *     kv_len == 0) has output 0 and log-sum-exp -inf (z_h with a sink).
  *   - Non-causal attention (the [MM] kernel) sees every key j < kv_len.
  *   - kv head of q head h is h / (num_q_heads / num_kv_heads).
  */
@@ -210,6 +224,10 @@ typedef struct {
     int32_t causal, dtype;
     int32_t variant;             /* 0 direct, 1 streaming, 2 split */
     int32_t param;               /* tile width (streaming) or parts (split) */
+    int32_t win_left, win_right; /* sliding window, -1 = unbounded */
+    double softcap;              /* 0 = off */
+    const double *alibi;         /* [Hq] slopes or NULL */
+    const double *sinks;         /* [Hq] sink logits or NULL */
     const int64_t *rows;         /* optional list of row ids t*Hq + h */
     int64_t n_rows;
     double *out;                 /* [n_rows, d] */
@@ -256,34 +274,40 @@ static void one_row(const problem_t *p, int64_t t, int32_t h, double *o,
     int32_t kvh = h / (p->Hq / p->Hkv);
 
     /* visible keys: j < Sk, and for causal j <= i + (Sk - Sq) (bottom-right
-     * alignment: the masked set is triu(diagonal = Sk - Sq + 1)) */
-    int64_t limit = Sk;
-    if (p->causal) {
-        int64_t last = i + (Sk - Sq);
-        if (last + 1 < limit) limit = last + 1;
-    }
+     * alignment: the masked set is triu(diagonal = Sk - Sq + 1)); a sliding
+     * window narrows the range to [diag - W_l, diag + W_r] */
+    const int64_t diag = i + (Sk - Sq);
+    int64_t lo = 0, limit = Sk;
+    if (p->causal && diag + 1 < limit) limit = diag + 1;
+    if (p->win_right >= 0 && diag + p->win_right + 1 < limit) limit = diag + p->win_right + 1;
+    if (p->win_left >= 0 && diag - p->win_left > lo) lo = diag - p->win_left;
+    const double sink = p->sinks ? p->sinks[h] : -INFINITY;
     for (int32_t c = 0; c < d; ++c) o[c] = 0.0;
-    if (limit <= 0) {
-        if (lse) *lse = -INFINITY;
+    if (limit <= lo) {
+        if (lse) *lse = sink;      /* -inf without a sink */
         return;
     }
     for (int32_t c = 0; c < d; ++c)
         qv[c] = oracle_widen16(p->q[(t * p->Hq + h) * (int64_t)d + c], p->dtype);
 
-    /* scores s_j = tau * <q, K_j> */
-    for (int64_t j = 0; j < limit; ++j) {
+    /* scores s_j = tau * <q, K_j>, then the softcap and the ALiBi bias */
+    for (int64_t j = lo; j < limit; ++j) {
         double acc = 0.0;
         for (int32_t c = 0; c < d; ++c)
             acc += qv[c] * cache_at(p, p->k_cache, b, j, kvh, c);
-        s[j] = p->scale * acc;
+        double x = p->scale * acc;
+        if (p->softcap > 0.0) x = p->softcap * tanh(x / p->softcap);
+        if (p->alibi) x -= p->alibi[h] * fabs((double)(diag - j));
+        s[j] = x;
     }
 
     if (p->variant == 0) {
-        /* [ALG] sec. 1-2: weights e^(s_j - max) / sum, output sum of w_j V_j */
-        double m = -INFINITY;
-        for (int64_t j = 0; j < limit; ++j) if (s[j] > m) m = s[j];
-        double den = 0.0;
-        for (int64_t j = 0; j < limit; ++j) {
+        /* [ALG] sec. 1-2: weights e^(s_j - max) / sum, output sum of w_j V_j;
+         * a sink adds e^(z - max) to the sum only */
+        double m = sink;
+        for (int64_t j = lo; j < limit; ++j) if (s[j] > m) m = s[j];
+        double den = p->sinks ? exp(sink - m) : 0.0;
+        for (int64_t j = lo; j < limit; ++j) {
             double w = exp(s[j] - m);
             den += w;
             for (int32_t c = 0; c < d; ++c)
@@ -377,6 +401,11 @@ static int run_problem(problem_t *p, int32_t n_threads)
     if (p->Hkv <= 0 || p->Hq % p->Hkv != 0 || p->d <= 0 || p->bs <= 0) return 1;
     if (p->variant == 2 && (p->param < 1 || p->param > 256)) return 1;
     if (p->variant == 1 && p->param < 1) return 1;
+    /* the self-test variants take the plain problem only */
+    if (p->variant != 0 && (p->win_left >= 0 || p->win_right >= 0 || p->softcap != 0.0 ||
+                            p->alibi || p->sinks))
+        return 1;
+    if (!(p->softcap >= 0.0) || p->win_left < -1 || p->win_right < -1) return 1;
     int64_t total_q = p->query_start_loc[p->num_seqs];
     if (!p->rows) p->n_rows = total_q * p->Hq;
     p->max_kv = 0;
@@ -408,18 +437,23 @@ static int run_problem(problem_t *p, int32_t n_threads)
 }
 
 /* Common entry.  out is [n_rows, d] (n_rows = total_q * Hq when rows is
- * NULL, in (token, head) order), lse is [n_rows] or NULL. */
-int oracle_sdpa_run(double *out, double *lse,
-                    const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
-                    const int32_t *block_table, int32_t bt_stride,
-                    const int32_t *query_start_loc, const int32_t *seq_lens,
-                    int32_t num_seqs, int32_t Hq, int32_t Hkv, int32_t d, int32_t bs,
-                    double scale, int32_t causal, int32_t dtype,
-                    int32_t variant, int32_t param,
-                    const int64_t *rows, int64_t n_rows, int32_t n_threads)
+ * NULL, in (token, head) order), lse is [n_rows] or NULL.  win_left /
+ * win_right = -1, softcap = 0, alibi = sinks = NULL give the plain problem. */
+int oracle_sdpa_run_ex(double *out, double *lse,
+                       const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
+                       const int32_t *block_table, int32_t bt_stride,
+                       const int32_t *query_start_loc, const int32_t *seq_lens,
+                       int32_t num_seqs, int32_t Hq, int32_t Hkv, int32_t d, int32_t bs,
+                       double scale, int32_t causal, int32_t dtype,
+                       int32_t variant, int32_t param,
+                       const int64_t *rows, int64_t n_rows, int32_t n_threads,
+                       int32_t win_left, int32_t win_right, double softcap,
+                       const double *alibi, const double *sinks)
 {
     problem_t p;
     memset(&p, 0, sizeof(p));
+    p.win_left = win_left; p.win_right = win_right; p.softcap = softcap;
+    p.alibi = alibi; p.sinks = sinks;
     p.q = q; p.k_cache = k_cache; p.v_cache = v_cache;
     p.block_table = block_table; p.bt_stride = bt_stride;
     p.query_start_loc = query_start_loc; p.seq_lens = seq_lens;
@@ -429,4 +463,19 @@ int oracle_sdpa_run(double *out, double *lse,
     p.rows = rows; p.n_rows = n_rows;
     p.out = out; p.lse = lse;
     return run_problem(&p, n_threads);
+}
+
+int oracle_sdpa_run(double *out, double *lse,
+                    const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
+                    const int32_t *block_table, int32_t bt_stride,
+                    const int32_t *query_start_loc, const int32_t *seq_lens,
+                    int32_t num_seqs, int32_t Hq, int32_t Hkv, int32_t d, int32_t bs,
+                    double scale, int32_t causal, int32_t dtype,
+                    int32_t variant, int32_t param,
+                    const int64_t *rows, int64_t n_rows, int32_t n_threads)
+{
+    return oracle_sdpa_run_ex(out, lse, q, k_cache, v_cache, block_table, bt_stride,
+                              query_start_loc, seq_lens, num_seqs, Hq, Hkv, d, bs, scale,
+                              causal, dtype, variant, param, rows, n_rows, n_threads,
+                              -1, -1, 0.0, NULL, NULL);
 }

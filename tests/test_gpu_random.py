@@ -1,6 +1,6 @@
 """Randomised parity sweep: seeded random paged problems over every supported
 axis -- ragged batches (including empty query ranges and zero-length KV),
-every supported block size, GQA groups odd and even, head size 64 and 128,
+every supported block size, GQA groups odd and even, head sizes 64, 128 and 256,
 fp16 and bf16, causal and non-causal, all output roundings -- each compared
 element by element with the fp64 oracle and, where asked, its log-sum-exp.
 Sizes are kept small enough for the oracle to check every row.
@@ -40,10 +40,11 @@ def check(prob, got, ref, rounding):
     assert err <= bound, (err, worst(got, ref))
 
 
-def random_prefill(seed):
+def random_prefill(seed, head_size=None):
     rng = np.random.default_rng(seed)
     hq, hkv = GROUPS[rng.integers(len(GROUPS))]
     d = int(rng.choice([64, 128]))
+    d = head_size or d
     dtype = torch.bfloat16 if rng.random() < 0.6 else torch.float16
     causal = bool(rng.random() < 0.7)
     n = int(rng.integers(1, 5))
@@ -66,8 +67,16 @@ def random_prefill(seed):
 
 @pytest.mark.parametrize("seed", range(24))
 def test_random_prefill(seed):
-    prob = random_prefill(1000 + seed)
-    rounding = seed % 4                       # RTNE, RTNA, RTZ, fp32 output
+    check_random_prefill(random_prefill(1000 + seed), seed % 4)
+
+
+@pytest.mark.parametrize("seed", range(10))
+def test_random_prefill_d256(seed):
+    check_random_prefill(random_prefill(3000 + seed, head_size=256), seed % 4)
+
+
+def check_random_prefill(prob, rounding):
+    """rounding: 0 RTNE, 1 RTNA, 2 RTZ, 3 fp32 output."""
     out, lse = gpu_prefill(prob, rounding=rounding, lse=True)
     torch.cuda.synchronize()
     ref, ref_lse = oracle_run(prob)
@@ -80,10 +89,11 @@ def test_random_prefill(seed):
         assert np.max(np.abs(g[finite] - ref_lse[finite])) < 2e-3
 
 
-def random_decode(seed):
+def random_decode(seed, head_size=None):
     rng = np.random.default_rng(seed)
     hq, hkv = GROUPS[rng.integers(len(GROUPS))]
     d = int(rng.choice([64, 128]))
+    d = head_size or d
     dtype = torch.bfloat16 if rng.random() < 0.6 else torch.float16
     n = int(rng.integers(1, 12))
     kv_lens = [int(rng.choice([0, int(rng.integers(1, 40)), int(rng.integers(40, 3000))]))
@@ -97,7 +107,15 @@ def random_decode(seed):
 
 @pytest.mark.parametrize("seed", range(16))
 def test_random_decode(seed):
-    prob = random_decode(2000 + seed)
+    check_random_decode(random_decode(2000 + seed), seed)
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_random_decode_d256(seed):
+    check_random_decode(random_decode(4000 + seed, head_size=256), seed)
+
+
+def check_random_decode(prob, seed):
     splits = int(np.random.default_rng(seed).choice([1, 2, 3, 8, 13]))
     out = gpu_decode(prob, splits=splits, rounding=seed % 4)
     torch.cuda.synchronize()
