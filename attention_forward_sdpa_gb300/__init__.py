@@ -8,10 +8,16 @@ kernels; there is no fallback of any kind.  If the library has not been built
 (``python -m attention_forward_sdpa_gb300.build_ext``) every call raises.
 
 Entry points (same names as the C functions):
-  attn_fwd_prefill, attn_fwd_decode, attn_fwd_decode_noalloc, attn_decode_workspace_size,
-  attn_round_f32, attn_status_string, attn_abi_version
-and allocating conveniences ``prefill`` and ``decode`` that create the output
-(and the decode workspace) with torch on the inputs' device.
+  attn_fwd_prefill, attn_fwd_dense, attn_fwd_decode, attn_fwd_decode_noalloc,
+  attn_decode_workspace_size, attn_round_f32, attn_status_string, attn_abi_version
+and allocating conveniences ``prefill``, ``dense`` and ``decode`` that create
+the output (and the decode workspace) with torch on the inputs' device.
+
+Feature flags (the C calls attn_fwd_prefill_ex / attn_fwd_dense_ex /
+attn_fwd_decode_ex, used when any flag is given): ``window=(left, right)``
+sliding window around the aligned key (-1 = unbounded), ``softcap`` > 0,
+``alibi_slopes`` and ``sinks`` as CUDA fp32 tensors with one entry per query
+head.  Their definitions are in include/attn_fwd.h.
 """
 from __future__ import annotations
 
@@ -23,7 +29,8 @@ import torch
 
 from .build_ext import LIB_PATH
 
-__all__ = ["attn_fwd_prefill", "attn_fwd_decode", "attn_fwd_decode_noalloc",
+__all__ = ["attn_fwd_prefill", "attn_fwd_dense", "attn_fwd_decode", "attn_fwd_decode_noalloc",
+           "has_features", "dense",
            "attn_decode_workspace_size",
            "attn_round_f32", "attn_status_string", "attn_abi_version", "prefill", "decode",
            "AttnError", "library_path", "load_library", "RTNE", "RTNA", "RTZ", "OUT_F32"]
@@ -82,6 +89,13 @@ def load_library() -> ctypes.CDLL:
         lib.attn_fwd_decode_noalloc.argtypes = [P, P, P, P, P, i32, P, i32, i32, i32, i32, i32,
                                                 i32, i32, f32, i32, ctypes.c_int, ctypes.c_int, P,
                                                 P, P]
+        FP = ctypes.POINTER(_Features)
+        lib.attn_fwd_prefill_ex.restype = ctypes.c_int
+        lib.attn_fwd_prefill_ex.argtypes = list(lib.attn_fwd_prefill.argtypes) + [FP]
+        lib.attn_fwd_dense_ex.restype = ctypes.c_int
+        lib.attn_fwd_dense_ex.argtypes = list(lib.attn_fwd_dense.argtypes) + [FP]
+        lib.attn_fwd_decode_ex.restype = ctypes.c_int
+        lib.attn_fwd_decode_ex.argtypes = list(lib.attn_fwd_decode.argtypes) + [FP]
         lib.attn_round_f32.restype = ctypes.c_int
         lib.attn_round_f32.argtypes = [P, P, i64, ctypes.c_int, ctypes.c_int, P]
         lib.attn_status_string.restype = ctypes.c_char_p
@@ -135,6 +149,34 @@ def _check(rc: int, where: str):
         raise AttnError(rc, where)
 
 
+class _Features(ctypes.Structure):
+    """attn_features_t"""
+    _fields_ = [("window_left", ctypes.c_int32), ("window_right", ctypes.c_int32),
+                ("softcap", ctypes.c_float), ("alibi_slopes", ctypes.c_void_p),
+                ("sinks", ctypes.c_void_p)]
+
+
+def _features(num_q_heads: int, window=None, softcap: float = 0.0, alibi_slopes=None,
+              sinks=None):
+    """The attn_features_t of a call, or None for a plain call."""
+    if window is None and not softcap and alibi_slopes is None and sinks is None:
+        return None
+    wl, wr = (-1, -1) if window is None else (int(window[0]), int(window[1]))
+    for t, name in ((alibi_slopes, "alibi_slopes"), (sinks, "sinks")):
+        if t is not None:
+            _dev(t, name, torch.float32)
+            if t.numel() != num_q_heads:
+                raise ValueError(f"{name} needs one entry per query head ({num_q_heads})")
+    return _Features(wl, wr, float(softcap),
+                     None if alibi_slopes is None else alibi_slopes.data_ptr(),
+                     None if sinks is None else sinks.data_ptr())
+
+
+def has_features(window=None, softcap: float = 0.0, alibi_slopes=None, sinks=None) -> bool:
+    """True when a call carries any feature flag."""
+    return not (window is None and not softcap and alibi_slopes is None and sinks is None)
+
+
 # ----------------------------------------------------------------------------
 # C entry points
 # ----------------------------------------------------------------------------
@@ -155,8 +197,10 @@ def attn_decode_workspace_size(num_seqs: int, num_q_heads: int, head_size: int,
 
 def attn_fwd_prefill(out, q, k_cache, v_cache, block_table, query_start_loc, seq_lens, *,
                      max_seqlen_q: int, max_seqlen_k: int, scale: float, causal: bool,
-                     rounding: int = RTNE, lse=None, status=None, stream=None) -> None:
-    """Calls attn_fwd_prefill on torch CUDA tensors (shapes as in the C header)."""
+                     rounding: int = RTNE, lse=None, status=None, stream=None, window=None,
+                     softcap: float = 0.0, alibi_slopes=None, sinks=None) -> None:
+    """Calls attn_fwd_prefill (attn_fwd_prefill_ex with feature flags) on torch
+    CUDA tensors (shapes as in the C header)."""
     lib = load_library()
     dt = _dtype_code(q.dtype)
     _dev(q, "q")
@@ -178,12 +222,15 @@ def attn_fwd_prefill(out, q, k_cache, v_cache, block_table, query_start_loc, seq
     if query_start_loc.shape[0] != num_seqs + 1 or block_table.dim() != 2 or \
             block_table.shape[0] != num_seqs:
         raise ValueError("inconsistent query_start_loc / block_table / seq_lens shapes")
-    rc = lib.attn_fwd_prefill(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table),
-                              block_table.shape[1], _ptr(query_start_loc), _ptr(seq_lens),
-                              num_seqs, int(max_seqlen_q), int(max_seqlen_k), total_q, hq, hkv, d,
-                              bs, nb, float(scale), int(bool(causal)), dt, int(rounding),
-                              _ptr(lse), _ptr(status), _stream_handle(stream))
-    _check(rc, "attn_fwd_prefill")
+    args = (_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table),
+            block_table.shape[1], _ptr(query_start_loc), _ptr(seq_lens), num_seqs,
+            int(max_seqlen_q), int(max_seqlen_k), total_q, hq, hkv, d, bs, nb, float(scale),
+            int(bool(causal)), dt, int(rounding), _ptr(lse), _ptr(status), _stream_handle(stream))
+    feat = _features(hq, window, softcap, alibi_slopes, sinks)
+    if feat is None:
+        _check(lib.attn_fwd_prefill(*args), "attn_fwd_prefill")
+    else:
+        _check(lib.attn_fwd_prefill_ex(*args, ctypes.byref(feat)), "attn_fwd_prefill_ex")
 
 
 def _strides3(t, name):
@@ -197,7 +244,8 @@ def _strides3(t, name):
 
 
 def attn_fwd_dense(out, q, k, v, *, scale: float, causal: bool, rounding: int = RTNE, lse=None,
-                   status=None, stream=None) -> None:
+                   status=None, stream=None, window=None, softcap: float = 0.0,
+                   alibi_slopes=None, sinks=None) -> None:
     """Calls attn_fwd_dense on logical [batch, seq, heads, head_size] CUDA
     tensors in any (batch, seq, head) stride order: BSHD tensors as they are,
     BHSD tensors x as x.transpose(1, 2) (a view, nothing is copied)."""
@@ -219,16 +267,22 @@ def attn_fwd_dense(out, q, k, v, *, scale: float, causal: bool, rounding: int = 
     b2, sk, hkv, d2 = k.shape
     if b2 != b or d2 != d or tuple(v.shape) != tuple(k.shape) or tuple(out.shape) != tuple(q.shape):
         raise ValueError("inconsistent q / k / v / out shapes")
-    rc = lib.attn_fwd_dense(_ptr(out), _ptr(q), _ptr(k), _ptr(v), qs, ks, vs, os_, b, sq, sk, hq,
-                            hkv, d, float(scale), int(bool(causal)), dt, int(rounding), _ptr(lse),
-                            _ptr(status), _stream_handle(stream))
-    _check(rc, "attn_fwd_dense")
+    args = (_ptr(out), _ptr(q), _ptr(k), _ptr(v), qs, ks, vs, os_, b, sq, sk, hq, hkv, d,
+            float(scale), int(bool(causal)), dt, int(rounding), _ptr(lse), _ptr(status),
+            _stream_handle(stream))
+    feat = _features(hq, window, softcap, alibi_slopes, sinks)
+    if feat is None:
+        _check(lib.attn_fwd_dense(*args), "attn_fwd_dense")
+    else:
+        _check(lib.attn_fwd_dense_ex(*args, ctypes.byref(feat)), "attn_fwd_dense_ex")
 
 
 def attn_fwd_decode(out, q, k_cache, v_cache, block_table, seq_lens, *, max_seqlen_k: int,
                     scale: float, num_splits: int, workspace=None, rounding: int = RTNE,
-                    lse=None, status=None, stream=None) -> None:
-    """Calls attn_fwd_decode on torch CUDA tensors (shapes as in the C header)."""
+                    lse=None, status=None, stream=None, window=None, softcap: float = 0.0,
+                    alibi_slopes=None, sinks=None) -> None:
+    """Calls attn_fwd_decode (attn_fwd_decode_ex with feature flags) on torch
+    CUDA tensors (shapes as in the C header)."""
     lib = load_library()
     dt = _dtype_code(q.dtype)
     _dev(q, "q")
@@ -251,12 +305,15 @@ def attn_fwd_decode(out, q, k_cache, v_cache, block_table, seq_lens, *, max_seql
         raise ValueError("inconsistent q / k_cache / v_cache / out shapes")
     if seq_lens.shape[0] != num_seqs or block_table.dim() != 2 or block_table.shape[0] != num_seqs:
         raise ValueError("inconsistent block_table / seq_lens shapes")
-    rc = lib.attn_fwd_decode(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table),
-                             block_table.shape[1], _ptr(seq_lens), num_seqs, int(max_seqlen_k), hq,
-                             hkv, d, bs, nb, float(scale), int(num_splits), dt, int(rounding),
-                             _ptr(lse), _ptr(workspace), ws_bytes, _ptr(status),
-                             _stream_handle(stream))
-    _check(rc, "attn_fwd_decode")
+    args = (_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table),
+            block_table.shape[1], _ptr(seq_lens), num_seqs, int(max_seqlen_k), hq, hkv, d, bs, nb,
+            float(scale), int(num_splits), dt, int(rounding), _ptr(lse), _ptr(workspace),
+            ws_bytes, _ptr(status), _stream_handle(stream))
+    feat = _features(hq, window, softcap, alibi_slopes, sinks)
+    if feat is None:
+        _check(lib.attn_fwd_decode(*args), "attn_fwd_decode")
+    else:
+        _check(lib.attn_fwd_decode_ex(*args, ctypes.byref(feat)), "attn_fwd_decode_ex")
 
 
 def attn_fwd_decode_noalloc(out, q, k_cache, v_cache, block_table, seq_lens, *,
@@ -310,8 +367,10 @@ def attn_round_f32(out, x, *, dtype: torch.dtype, rounding: int, stream=None) ->
 
 def prefill(q, k_cache, v_cache, block_table, query_start_loc, seq_lens, *, max_seqlen_q: int,
             max_seqlen_k: int, scale: float | None = None, causal: bool = True,
-            rounding: int = RTNE, return_lse: bool = False, status=None, stream=None):
-    """Returns O (and the log-sum-exp when asked) for a paged prefill problem."""
+            rounding: int = RTNE, return_lse: bool = False, status=None, stream=None,
+            **features):
+    """Returns O (and the log-sum-exp when asked) for a paged prefill problem.
+    ``features``: window, softcap, alibi_slopes, sinks (see the module doc)."""
     if scale is None:
         scale = q.shape[-1] ** -0.5
     out = torch.empty(q.shape, dtype=torch.float32 if rounding == OUT_F32 else q.dtype,
@@ -319,12 +378,13 @@ def prefill(q, k_cache, v_cache, block_table, query_start_loc, seq_lens, *, max_
     lse = torch.empty(q.shape[:2], dtype=torch.float32, device=q.device) if return_lse else None
     attn_fwd_prefill(out, q, k_cache, v_cache, block_table, query_start_loc, seq_lens,
                      max_seqlen_q=max_seqlen_q, max_seqlen_k=max_seqlen_k, scale=scale,
-                     causal=causal, rounding=rounding, lse=lse, status=status, stream=stream)
+                     causal=causal, rounding=rounding, lse=lse, status=status, stream=stream,
+                     **features)
     return (out, lse) if return_lse else out
 
 
 def dense(q, k, v, *, layout: str = "bshd", scale: float | None = None, causal: bool = False,
-          rounding: int = RTNE, return_lse: bool = False, status=None, stream=None):
+          rounding: int = RTNE, return_lse: bool = False, status=None, stream=None, **features):
     """Returns O in the layout of q for fixed-length batches: layout "bshd"
     takes [B, S, H, d] tensors, "bhsd" takes [B, H, S, d] tensors (read in
     place).  The log-sum-exp, when asked, is [B, H, Sq] fp32."""
@@ -339,13 +399,13 @@ def dense(q, k, v, *, layout: str = "bshd", scale: float | None = None, causal: 
     lse = (torch.empty((qv.shape[0], qv.shape[2], qv.shape[1]), dtype=torch.float32,
                        device=q.device) if return_lse else None)
     attn_fwd_dense(view(out), qv, view(k), view(v), scale=scale, causal=causal, rounding=rounding,
-                   lse=lse, status=status, stream=stream)
+                   lse=lse, status=status, stream=stream, **features)
     return (out, lse) if return_lse else out
 
 
 def decode(q, k_cache, v_cache, block_table, seq_lens, *, max_seqlen_k: int,
            scale: float | None = None, num_splits: int = 8, rounding: int = RTNE,
-           return_lse: bool = False, workspace=None, status=None, stream=None):
+           return_lse: bool = False, workspace=None, status=None, stream=None, **features):
     """Returns O (and the log-sum-exp when asked) for one decode step."""
     if scale is None:
         scale = q.shape[-1] ** -0.5
@@ -357,5 +417,5 @@ def decode(q, k_cache, v_cache, block_table, seq_lens, *, max_seqlen_k: int,
         workspace = torch.empty(max(n, 16), dtype=torch.uint8, device=q.device) if n else None
     attn_fwd_decode(out, q, k_cache, v_cache, block_table, seq_lens, max_seqlen_k=max_seqlen_k,
                     scale=scale, num_splits=num_splits, workspace=workspace, rounding=rounding,
-                    lse=lse, status=status, stream=stream)
+                    lse=lse, status=status, stream=stream, **features)
     return (out, lse) if return_lse else out

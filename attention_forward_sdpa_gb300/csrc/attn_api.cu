@@ -58,6 +58,41 @@ bool valid_scale(float s) { return std::isfinite(s) && s > 0.f; }
 
 constexpr float kLog2e = 1.4426950408889634f;
 
+// The feature flags of attn_features_t, validated (NULL = none).
+struct Features {
+  int32_t win_left = -1, win_right = -1;
+  float softcap = 0.f;
+  const float* alibi = nullptr;
+  const float* sinks = nullptr;
+  bool any() const { return win_left >= 0 || win_right >= 0 || softcap > 0.f || alibi || sinks; }
+};
+
+attn_status_t read_features(const attn_features_t* f, Features& out) {
+  out = Features();
+  if (!f) return ATTN_OK;
+  if (f->window_left < -1 || f->window_right < -1) return ATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(f->softcap) || f->softcap < 0.f) return ATTN_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(f->alibi_slopes) & 3u) ||
+      (reinterpret_cast<uintptr_t>(f->sinks) & 3u))
+    return ATTN_ERR_INVALID_ARG;
+  out.win_left = f->window_left;
+  out.win_right = f->window_right;
+  out.softcap = f->softcap;
+  out.alibi = f->alibi_slopes;
+  out.sinks = f->sinks;
+  return ATTN_OK;
+}
+
+void set_features(attn::PrefillParams& p, const Features& f, float scale) {
+  p.win_left = f.win_left;
+  p.win_right = f.win_right;
+  p.softcap = f.softcap;
+  p.alibi = f.alibi;
+  p.sinks = f.sinks;
+  p.scale = scale;
+  p.score_xform = (f.softcap > 0.f || f.alibi) ? 1 : 0;
+}
+
 // Prefill grid (x: head units, z: row units; y is the sequence).  Head sizes
 // 64 and 128 put two 128-row query tiles in a CTA: two heads of a GQA group
 // when the group size is even, else two row blocks of one head.  Head size
@@ -119,7 +154,8 @@ int decode_prepare_and_launch(DecodeParams& p, int head_size, bool bf16, void* w
   }
   const int G = p.num_q_heads / p.num_kv_heads;
   const bool pow2 = (G & (G - 1)) == 0;
-  const bool tc_path = head_size == 128 && ((G <= 16 && pow2) || G % 16 == 0);
+  const bool features = p.win_left >= 0 || p.score_xform || p.sinks;
+  const bool tc_path = head_size == 128 && ((G <= 16 && pow2) || G % 16 == 0) && !features;
   if (!tc_path) {
     cudaError_t e = launch_decode(p, head_size, bf16, G, stream);
     return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
@@ -206,8 +242,11 @@ attn_status_t prefill_impl(void* out, const void* q, const void* k_cache, const 
                            int32_t head_size, int32_t block_size, int32_t num_blocks, float scale,
                            int32_t causal, attn_dtype_t dtype, attn_round_t rounding,
                            float* lse_out, int32_t* status_dev, void* stream,
-                           uint64_t wait_limit_ns, int32_t stall_producer) {
+                           uint64_t wait_limit_ns, int32_t stall_producer,
+                           const attn_features_t* features) {
   // ---- host-side validation (no CUDA call before this block ends)
+  Features feat;
+  if (read_features(features, feat) != ATTN_OK) return ATTN_ERR_INVALID_ARG;
   if (num_seqs < 0 || max_seqlen_q < 0 || max_seqlen_k < 0 || total_q < 0) return ATTN_ERR_INVALID_ARG;
   if (num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0) return ATTN_ERR_INVALID_ARG;
   if (dtype != ATTN_F16 && dtype != ATTN_BF16) return ATTN_ERR_INVALID_ARG;
@@ -282,6 +321,7 @@ attn_status_t prefill_impl(void* out, const void* q, const void* k_cache, const 
   p.scale_log2 = scale * kLog2e;
   p.wait_limit_ns = wait_limit_ns;
   p.stall_producer = stall_producer;
+  set_features(p, feat, scale);
 
   dim3 grid((unsigned)gx, (unsigned)num_seqs, (unsigned)gz);
   cudaError_t e = attn::launch_prefill(p, head_size, bf16, grid, static_cast<cudaStream_t>(stream));
@@ -301,7 +341,23 @@ attn_status_t attn_fwd_prefill(void* out, const void* q, const void* k_cache, co
   return prefill_impl(out, q, k_cache, v_cache, block_table, block_table_stride, query_start_loc,
                       seq_lens, num_seqs, max_seqlen_q, max_seqlen_k, total_q, num_q_heads,
                       num_kv_heads, head_size, block_size, num_blocks, scale, causal, dtype,
-                      rounding, lse_out, status_dev, stream, kDefaultWaitLimitNs, 0);
+                      rounding, lse_out, status_dev, stream, kDefaultWaitLimitNs, 0, nullptr);
+}
+
+attn_status_t attn_fwd_prefill_ex(void* out, const void* q, const void* k_cache,
+                                  const void* v_cache, const int32_t* block_table,
+                                  int32_t block_table_stride, const int32_t* query_start_loc,
+                                  const int32_t* seq_lens, int32_t num_seqs, int32_t max_seqlen_q,
+                                  int32_t max_seqlen_k, int32_t total_q, int32_t num_q_heads,
+                                  int32_t num_kv_heads, int32_t head_size, int32_t block_size,
+                                  int32_t num_blocks, float scale, int32_t causal,
+                                  attn_dtype_t dtype, attn_round_t rounding, float* lse_out,
+                                  int32_t* status_dev, void* stream,
+                                  const attn_features_t* features) {
+  return prefill_impl(out, q, k_cache, v_cache, block_table, block_table_stride, query_start_loc,
+                      seq_lens, num_seqs, max_seqlen_q, max_seqlen_k, total_q, num_q_heads,
+                      num_kv_heads, head_size, block_size, num_blocks, scale, causal, dtype,
+                      rounding, lse_out, status_dev, stream, kDefaultWaitLimitNs, 0, features);
 }
 
 attn_status_t attn_test_prefill_timeout(void* out, const void* q, const void* k_cache,
@@ -319,17 +375,20 @@ attn_status_t attn_test_prefill_timeout(void* out, const void* q, const void* k_
   return prefill_impl(out, q, k_cache, v_cache, block_table, block_table_stride, query_start_loc,
                       seq_lens, num_seqs, max_seqlen_q, max_seqlen_k, total_q, num_q_heads,
                       num_kv_heads, head_size, block_size, num_blocks, scale, causal, dtype,
-                      rounding, nullptr, status_dev, stream, wait_limit_ns, 1);
+                      rounding, nullptr, status_dev, stream, wait_limit_ns, 1, nullptr);
 }
 
-attn_status_t attn_fwd_dense(void* out, const void* q, const void* k, const void* v,
-                             const int64_t* q_strides, const int64_t* k_strides,
-                             const int64_t* v_strides, const int64_t* o_strides, int32_t batch,
-                             int32_t seqlen_q, int32_t seqlen_k, int32_t num_q_heads,
-                             int32_t num_kv_heads, int32_t head_size, float scale, int32_t causal,
-                             attn_dtype_t dtype, attn_round_t rounding, float* lse_out,
-                             int32_t* status_dev, void* stream) {
+attn_status_t attn_fwd_dense_ex(void* out, const void* q, const void* k, const void* v,
+                                const int64_t* q_strides, const int64_t* k_strides,
+                                const int64_t* v_strides, const int64_t* o_strides, int32_t batch,
+                                int32_t seqlen_q, int32_t seqlen_k, int32_t num_q_heads,
+                                int32_t num_kv_heads, int32_t head_size, float scale,
+                                int32_t causal, attn_dtype_t dtype, attn_round_t rounding,
+                                float* lse_out, int32_t* status_dev, void* stream,
+                                const attn_features_t* features) {
   // ---- host-side validation (no CUDA call before this block ends)
+  Features feat;
+  if (read_features(features, feat) != ATTN_OK) return ATTN_ERR_INVALID_ARG;
   if (batch < 0 || seqlen_q < 0 || seqlen_k < 0) return ATTN_ERR_INVALID_ARG;
   if (num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0) return ATTN_ERR_INVALID_ARG;
   if (dtype != ATTN_F16 && dtype != ATTN_BF16) return ATTN_ERR_INVALID_ARG;
@@ -410,10 +469,23 @@ attn_status_t attn_fwd_dense(void* out, const void* q, const void* k, const void
   p.rounding = (int32_t)rounding;
   p.scale_log2 = scale * kLog2e;
   p.wait_limit_ns = kDefaultWaitLimitNs;
+  set_features(p, feat, scale);
 
   dim3 grid((unsigned)gx, (unsigned)batch, (unsigned)gz);
   cudaError_t e = attn::launch_prefill(p, head_size, bf16, grid, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+attn_status_t attn_fwd_dense(void* out, const void* q, const void* k, const void* v,
+                             const int64_t* q_strides, const int64_t* k_strides,
+                             const int64_t* v_strides, const int64_t* o_strides, int32_t batch,
+                             int32_t seqlen_q, int32_t seqlen_k, int32_t num_q_heads,
+                             int32_t num_kv_heads, int32_t head_size, float scale, int32_t causal,
+                             attn_dtype_t dtype, attn_round_t rounding, float* lse_out,
+                             int32_t* status_dev, void* stream) {
+  return attn_fwd_dense_ex(out, q, k, v, q_strides, k_strides, v_strides, o_strides, batch,
+                           seqlen_q, seqlen_k, num_q_heads, num_kv_heads, head_size, scale, causal,
+                           dtype, rounding, lse_out, status_dev, stream, nullptr);
 }
 
 size_t attn_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t head_size,
@@ -425,14 +497,17 @@ size_t attn_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t
   return rows * (size_t)head_size * sizeof(float) + rows * 2 * sizeof(float) + counter_bytes;
 }
 
-attn_status_t attn_fwd_decode(void* out, const void* q, const void* k_cache, const void* v_cache,
-                              const int32_t* block_table, int32_t block_table_stride,
-                              const int32_t* seq_lens, int32_t num_seqs, int32_t max_seqlen_k,
-                              int32_t num_q_heads, int32_t num_kv_heads, int32_t head_size,
-                              int32_t block_size, int32_t num_blocks, float scale,
-                              int32_t num_splits, attn_dtype_t dtype, attn_round_t rounding,
-                              float* lse_out, void* workspace, size_t workspace_bytes,
-                              int32_t* status_dev, void* stream) {
+attn_status_t attn_fwd_decode_ex(void* out, const void* q, const void* k_cache,
+                                 const void* v_cache, const int32_t* block_table,
+                                 int32_t block_table_stride, const int32_t* seq_lens,
+                                 int32_t num_seqs, int32_t max_seqlen_k, int32_t num_q_heads,
+                                 int32_t num_kv_heads, int32_t head_size, int32_t block_size,
+                                 int32_t num_blocks, float scale, int32_t num_splits,
+                                 attn_dtype_t dtype, attn_round_t rounding, float* lse_out,
+                                 void* workspace, size_t workspace_bytes, int32_t* status_dev,
+                                 void* stream, const attn_features_t* features) {
+  Features feat;
+  if (read_features(features, feat) != ATTN_OK) return ATTN_ERR_INVALID_ARG;
   if (num_seqs < 0 || max_seqlen_k < 0) return ATTN_ERR_INVALID_ARG;
   if (num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0) return ATTN_ERR_INVALID_ARG;
   if (dtype != ATTN_F16 && dtype != ATTN_BF16) return ATTN_ERR_INVALID_ARG;
@@ -475,8 +550,28 @@ attn_status_t attn_fwd_decode(void* out, const void* q, const void* k_cache, con
   p.num_splits = num_splits;
   p.rounding = (int32_t)rounding;
   p.scale_log2 = scale * kLog2e;
+  p.scale = scale;
+  p.win_left = feat.win_left;      // the right bound never cuts a decode row (diag = kv_len - 1)
+  p.softcap = feat.softcap;
+  p.alibi = feat.alibi;
+  p.sinks = feat.sinks;
+  p.score_xform = (feat.softcap > 0.f || feat.alibi) ? 1 : 0;
   return (attn_status_t)attn::decode_prepare_and_launch(p, head_size, dtype == ATTN_BF16, workspace,
                                                         static_cast<cudaStream_t>(stream));
+}
+
+attn_status_t attn_fwd_decode(void* out, const void* q, const void* k_cache, const void* v_cache,
+                              const int32_t* block_table, int32_t block_table_stride,
+                              const int32_t* seq_lens, int32_t num_seqs, int32_t max_seqlen_k,
+                              int32_t num_q_heads, int32_t num_kv_heads, int32_t head_size,
+                              int32_t block_size, int32_t num_blocks, float scale,
+                              int32_t num_splits, attn_dtype_t dtype, attn_round_t rounding,
+                              float* lse_out, void* workspace, size_t workspace_bytes,
+                              int32_t* status_dev, void* stream) {
+  return attn_fwd_decode_ex(out, q, k_cache, v_cache, block_table, block_table_stride, seq_lens,
+                            num_seqs, max_seqlen_k, num_q_heads, num_kv_heads, head_size,
+                            block_size, num_blocks, scale, num_splits, dtype, rounding, lse_out,
+                            workspace, workspace_bytes, status_dev, stream, nullptr);
 }
 
 attn_status_t attn_round_f32(void* out, const float* in, int64_t n, attn_dtype_t dtype,

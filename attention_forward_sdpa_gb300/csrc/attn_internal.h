@@ -45,6 +45,15 @@ struct PrefillParams {
   float scale_log2;     // tau * log2(e)
   uint64_t wait_limit_ns;  // limit of every pipeline wait (the library default, or a test's)
   int32_t stall_producer;  // test only: the producer issues no copy, so the first wait runs out
+  // feature flags (attn_features_t): window bounds (-1 unbounded), softcap
+  // (0 off), per-head ALiBi slopes and sink logits (device, or nullptr)
+  int32_t win_left;
+  int32_t win_right;
+  int32_t score_xform;  // 1 when softcap or ALiBi rewrite the scores
+  float softcap;
+  float scale;          // tau, for the score rewrite
+  const float* alibi;
+  const float* sinks;
 };
 
 struct DecodeParams {
@@ -76,6 +85,14 @@ struct DecodeParams {
   int32_t num_splits;
   int32_t rounding;
   float scale_log2;
+  // feature flags, as in PrefillParams (the SIMT split kernel and the merge
+  // honour them; the tcgen05 decode kernel is not used when any is set)
+  int32_t win_left;
+  int32_t score_xform;
+  float softcap;
+  float scale;
+  const float* alibi;
+  const float* sinks;
 };
 
 // Launchers return a cudaError_t from the launch.

@@ -27,6 +27,7 @@
 
 #include "attn_internal.h"
 #include "round16.cuh"
+#include "score_features.cuh"
 #include "sm103_ptx.cuh"
 
 namespace attn {
@@ -157,8 +158,16 @@ __global__ void __launch_bounds__(kDecWarps * 32) decode_split_kernel(const __gr
     if (threadIdx.x == 0 && split == 0 && hg == 0) report_status(p.status, kStatusBadArg);
     return;
   }
+  // A sliding window keeps keys >= lo (the decode row's aligned key is
+  // Sk - 1); the splits cut [lo rounded down to 16, Sk) and keys below lo
+  // are masked, so chunks stay page-aligned.
+  const int lo = p.win_left >= 0 ? max(0, Sk - 1 - p.win_left) : 0;
+  const int lo16 = lo & ~15;
   int k_begin, k_end;
-  split_range(Sk, p.num_splits, split, k_begin, k_end);
+  split_range(Sk - lo16, p.num_splits, split, k_begin, k_end);
+  k_begin += lo16;
+  k_end += lo16;
+  const float inv_cap = p.softcap > 0.f ? 1.f / p.softcap : 0.f;
 
   const uint16_t* qb =
       static_cast<const uint16_t*>(p.q) + ((int64_t)b * p.num_q_heads + h0) * D + lane * DPL;
@@ -217,7 +226,15 @@ __global__ void __launch_bounds__(kDecWarps * 32) decode_split_kernel(const __gr
     for (int k = 0; k < NV; ++k) {
       const int idx = scatter_index<N>(lane, k);
       const int r = idx / GH, h = idx % GH;
-      s_sc[warp][r][h] = r < nv ? part[k] * sl2 : -INFINITY;
+      float sc = part[k] * sl2;
+      if (p.score_xform) {
+        // softcap / ALiBi on the scaled score, distance to the last key
+        const float slope = p.alibi ? p.alibi[h0 + h] : 0.f;
+        const float x = rewrite_score(part[k] * p.scale, p.softcap, inv_cap, slope,
+                                      (float)(Sk - 1 - (k0 + r)));
+        sc = x * 1.4426950408889634f;
+      }
+      s_sc[warp][r][h] = (r < nv && k0 + r >= lo) ? sc : -INFINITY;
     }
     __syncwarp();
 
@@ -296,9 +313,18 @@ __global__ void __launch_bounds__(kDecWarps * 32) decode_split_kernel(const __gr
     }
     const int64_t row = (int64_t)b * Hq + h0 + h;
     if (p.num_splits == 1) {
-      const float v = L > 0.f ? acc / L : 0.f;
+      float v, lse_v;
+      if (p.sinks) {
+        // the sink term joins the denominator here
+        float inv_l;
+        finish_row(M, L, p.sinks[h0 + h], inv_l, lse_v);
+        v = acc * inv_l;
+      } else {
+        v = L > 0.f ? acc / L : 0.f;
+        lse_v = L > 0.f ? M * kLn2 + logf(L) : -INFINITY;
+      }
       store_out<BF16>(p.out, row * D + e, &v, 1, p.rounding);
-      if (e == 0 && p.lse) p.lse[row] = L > 0.f ? M * kLn2 + logf(L) : -INFINITY;
+      if (e == 0 && p.lse) p.lse[row] = lse_v;
     } else {
       p.part_o[(row * p.num_splits + split) * D + e] = acc;
       if (e == 0) {
@@ -379,11 +405,15 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(const __grid_consta
 #pragma unroll
       for (int e = 0; e < DPL; ++e) acc[e] = fmaf(wg[u], v[u][e], acc[e]);
   }
-  const float inv = L > 0.f ? 1.f / L : 0.f;
+  // the weights are relative to 2^Mu: the merged state is (m, l) = (Mu, L),
+  // plus the sink term when the call has one
+  float inv, lse_v;
+  finish_row(M == -INFINITY ? -INFINITY : Mu, L, p.sinks ? p.sinks[row % p.num_q_heads] : -INFINITY,
+             inv, lse_v);
 #pragma unroll
   for (int e = 0; e < DPL; ++e) acc[e] *= inv;
   store_out<BF16>(p.out, row * D + lane * DPL, acc, DPL, p.rounding);
-  if (lane == 0 && p.lse) p.lse[row] = L > 0.f ? M * kLn2 + logf(L) : -INFINITY;
+  if (lane == 0 && p.lse) p.lse[row] = lse_v;
 }
 
 template <int D, bool BF16>

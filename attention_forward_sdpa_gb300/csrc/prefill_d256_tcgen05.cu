@@ -30,6 +30,7 @@
 
 #include "attn_internal.h"
 #include "round16.cuh"
+#include "score_features.cuh"
 #include "sm103_ptx.cuh"
 
 namespace attn {
@@ -52,7 +53,6 @@ constexpr int kMiscOff = kBarOff + kNumBars * 8;
 constexpr int kSmemBytes = kMiscOff + 16 + 1024;   // + slack for the 1024-byte alignment
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kOCol = 256;
-constexpr float kLn2 = 0.693147180559945309f;
 constexpr float kRescaleSlack = 8.f;     // log2 units: p stays <= 256
 
 static_assert(kSmemBytes <= 232448, "shared memory budget of one CTA");
@@ -64,8 +64,18 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint64
   }
 }
 
-template <bool BF16>
+// min(a, b + c) without int32 overflow (window bounds may be huge)
+__device__ __forceinline__ int min_sum(int a, int b, int c) {
+  const long long v = (long long)b + (long long)c;
+  return v < (long long)a ? (int)v : a;
+}
+
+// FEAT: the feature-flagged instantiation (sliding window, score rewrite,
+// sinks); without it the flags are compile-time off.
+template <bool BF16, bool FEAT>
 __global__ void __launch_bounds__(kThreads, 1) prefill_d256_kernel(const __grid_constant__ PrefillParams p) {
+  const int win_left = FEAT ? p.win_left : -1;
+  const int win_right = FEAT ? p.win_right : -1;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -108,9 +118,24 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_d256_kernel(const __grid_
   const int rows = min(kBM, Sq - row0);
   const int off = Sk - Sq;                                // row i sees keys j <= i + off
   const int last = row0 + rows - 1;
-  const int lim = p.causal ? min(Sk, last + off + 1) : Sk;
-  const int nkv = lim > 0 ? (lim + kBN - 1) / kBN : 0;
-  const int lim_lo = p.causal ? min(Sk, row0 + off + 1) : Sk;
+  // keys [lo, lim) of the tile's rows: the causal bound and a sliding window
+  // narrow them; lim_lo is the smallest upper limit and lo_hi the largest
+  // lower limit (tiles past lim_lo or before lo_hi need the element mask)
+  int lim = Sk, lim_lo = Sk, lo_first = 0, lo_hi = 0;
+  if (p.causal) {
+    lim = min(lim, last + off + 1);
+    lim_lo = min(lim_lo, row0 + off + 1);
+  }
+  if (win_right >= 0) {
+    lim = min_sum(lim, last + off + 1, win_right);
+    lim_lo = min_sum(lim_lo, row0 + off + 1, win_right);
+  }
+  if (win_left >= 0) {
+    lo_first = max(0, row0 + off - win_left);
+    lo_hi = max(0, last + off - win_left);
+  }
+  const int j0 = FEAT ? lo_first / kBN : 0;   // first key tile; tiles before it are skipped
+  const int nkv = lim > lo_first ? (lim + kBN - 1) / kBN - j0 : 0;   // key tiles from j0
   const int kvh = head / (p.num_q_heads / p.num_kv_heads);
 
   // ------------------------------------------------------------ setup
@@ -223,10 +248,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_d256_kernel(const __grid_
         }
         return true;
       };
-      for (int j = 0; ok && j < min(nkv, 2); ++j) ok = load_k(j, 0) && load_k(j, 1);
+      for (int j = 0; ok && j < min(nkv, 2); ++j) ok = load_k(j0 + j, 0) && load_k(j0 + j, 1);
       for (int j = 0; ok && j < nkv; ++j) {
-        ok = load_v(j, 0) && load_v(j, 1);
-        if (ok && j + 2 < nkv) ok = load_k(j + 2, 0) && load_k(j + 2, 1);
+        ok = load_v(j0 + j, 0) && load_v(j0 + j, 1);
+        if (ok && j + 2 < nkv) ok = load_k(j0 + j + 2, 0) && load_k(j0 + j + 2, 1);
       }
       // make sure no copy into this CTA's shared memory is still in flight
       for (int s = 0; s < kSlots; ++s)
@@ -292,7 +317,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_d256_kernel(const __grid_
       for (int h = 0; ok && h < 2; ++h) {
         int slot;
         if (!take(slot)) { ok = false; break; }
-        const int r0 = Sk - (j * kBN + 64 * h);      // rows >= r0 of this half lie past kv_len
+        const int r0 = Sk - ((j0 + j) * kBN + 64 * h);   // rows >= r0 of this half lie past kv_len
         if (r0 < 64) {
           // their V rows may hold anything (NaN included); P is 0 there but
           // 0 * NaN is not, so zero them
@@ -324,12 +349,16 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_d256_kernel(const __grid_
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
     const uint32_t tO = tmem + lane_off + kOCol;
     const int i_row = row0 + r;
-    const int key_lim = p.causal ? min(Sk, i_row + off + 1) : Sk;
+    int key_lim = p.causal ? min(Sk, i_row + off + 1) : Sk;
+    if (win_right >= 0) key_lim = min_sum(key_lim, i_row + off + 1, win_right);
+    const int key_lo = win_left >= 0 ? i_row + off - win_left : 0;
     const float sl2 = p.scale_log2;
+    const float slope = FEAT && p.alibi ? p.alibi[head] : 0.f;
     float m = -INFINITY, l = 0.f;
     bool ok = true;
     for (int j = 0; j < nkv; ++j) {
       const int buf = j & 1;
+      const int jk = j0 + j;                 // key tile
       const uint32_t tS = tmem + lane_off + 128u * buf;
       if (!mbar_wait(bar_s_full + 8u * buf, (j >> 1) & 1, abort_flag, p.wait_limit_ns)) { ok = false; break; }
       tc_fence_after();
@@ -338,13 +367,15 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_d256_kernel(const __grid_
       for (int c = 0; c < 4; ++c) tmem_ld32(tS + 32 * c, s[c]);
 #pragma unroll
       for (int c = 0; c < 4; ++c) tmem_ld_wait(s[c]);
-      if ((j + 1) * kBN > lim_lo) {
-        const int cl = key_lim - j * kBN;  // columns >= cl are masked for this row
+      if (FEAT && p.score_xform) rewrite_scores(s, p.scale, p.softcap, slope, (float)(i_row + off - jk * kBN));
+      if ((jk + 1) * kBN > lim_lo || (FEAT && jk * kBN < lo_hi)) {
+        const int cl = key_lim - jk * kBN;  // columns >= cl are masked for this row
+        const int cf = key_lo - jk * kBN;   // and columns < cf
 #pragma unroll
         for (int c = 0; c < 4; ++c)
 #pragma unroll
           for (int e = 0; e < 32; ++e)
-            if (32 * c + e >= cl) s[c][e] = 0xFF800000u;  // -inf
+            if (32 * c + e >= cl || (FEAT && 32 * c + e < cf)) s[c][e] = 0xFF800000u;  // -inf
       }
       float mc[4];
 #pragma unroll
@@ -412,7 +443,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_d256_kernel(const __grid_
     }
     const bool row_ok = r < rows;
     const int64_t tok = (int64_t)q_begin + row0 + r;
-    const float inv_l = l > 0.f ? 1.f / l : 0.f;
+    float inv_l, lse_v;
+    finish_row(m, l, FEAT && p.sinks ? p.sinks[head] : -INFINITY, inv_l, lse_v);
     // The Q buffer is free once o_full has fired (it covers every product
     // that read Q); the epilogue stages its output there.
     if (rows == kBM && p.rounding != 3) {
@@ -516,7 +548,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_d256_kernel(const __grid_
     if (ok && row_ok && p.lse) {
       const int64_t li = p.dense ? ((int64_t)b * p.num_q_heads + head) * Sq + row0 + r
                                  : tok * p.num_q_heads + head;
-      p.lse[li] = l > 0.f ? m * kLn2 + logf(l) : -INFINITY;
+      p.lse[li] = lse_v;
     }
   }
 
@@ -529,19 +561,21 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_d256_kernel(const __grid_
   if (threadIdx.x == 0 && *abort_flag) report_status(p.status, kStatusTimeout);
 }
 
-template <bool BF16>
+template <bool BF16, bool FEAT>
 cudaError_t launch_d256(const PrefillParams& p, dim3 grid, cudaStream_t stream) {
   static std::atomic<uint64_t> smem_set{0};
-  const cudaError_t e = ensure_dynamic_smem(prefill_d256_kernel<BF16>, kSmemBytes, smem_set);
+  const cudaError_t e = ensure_dynamic_smem(prefill_d256_kernel<BF16, FEAT>, kSmemBytes, smem_set);
   if (e != cudaSuccess) return e;
-  prefill_d256_kernel<BF16><<<grid, kThreads, kSmemBytes, stream>>>(p);
+  prefill_d256_kernel<BF16, FEAT><<<grid, kThreads, kSmemBytes, stream>>>(p);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_prefill_d256(const PrefillParams& p, bool bf16, dim3 grid, cudaStream_t stream) {
-  return bf16 ? launch_d256<true>(p, grid, stream) : launch_d256<false>(p, grid, stream);
+  const bool feat = p.win_left >= 0 || p.win_right >= 0 || p.score_xform || p.sinks;
+  if (feat) return bf16 ? launch_d256<true, true>(p, grid, stream) : launch_d256<false, true>(p, grid, stream);
+  return bf16 ? launch_d256<true, false>(p, grid, stream) : launch_d256<false, false>(p, grid, stream);
 }
 
 }  // namespace attn

@@ -34,6 +34,7 @@
 
 #include "attn_internal.h"
 #include "round16.cuh"
+#include "score_features.cuh"
 #include "sm103_ptx.cuh"
 
 namespace attn {
@@ -42,7 +43,6 @@ namespace {
 constexpr int kBM = 128;        // query rows per tile
 constexpr int kBN = 128;        // keys per KV tile
 constexpr int kThreads = 384;   // 12 warps
-constexpr float kLn2 = 0.693147180559945309f;
 constexpr float kRescaleSlack = 8.f;  // log2 units: p stays <= 256
 
 template <int D>
@@ -73,9 +73,20 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint64
   }
 }
 
-template <int D, bool BF16>
+// min(a, b + c) without int32 overflow (window bounds may be huge)
+__device__ __forceinline__ int min_sum(int a, int b, int c) {
+  const long long v = (long long)b + (long long)c;
+  return v < (long long)a ? (int)v : a;
+}
+
+// FEAT: the feature-flagged instantiation (sliding window, score rewrite,
+// sinks); without it the flags are compile-time off and the kernel carries
+// none of their registers.
+template <int D, bool BF16, bool FEAT>
 __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_constant__ PrefillParams p) {
   using L = PrefillLayout<D>;
+  const int win_left = FEAT ? p.win_left : -1;
+  const int win_right = FEAT ? p.win_right : -1;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -129,19 +140,47 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     }
   }
   const int off = Sk - Sq;  // bottom-right alignment: row i sees keys j <= i + off
+  // Per tile: keys [lo, lim) of its rows (a sliding window narrows both
+  // ends), the first key tile any row needs (jb), the end tile (n_kv), the
+  // smallest upper limit (lim_lo) and the largest lower limit (lo_hi) -- the
+  // tiles past lim_lo or before lo_hi need the per-element mask.
+  int jb[2], lo_hi[2];
 #pragma unroll
   for (int t = 0; t < 2; ++t) {
     rows[t] = row0[t] < Sq ? min(kBM, Sq - row0[t]) : 0;
     n_kv[t] = 0;
     lim_lo[t] = 0;
+    jb[t] = 0;
+    lo_hi[t] = 0;
     if (rows[t] > 0) {
       const int last = row0[t] + rows[t] - 1;
-      const int lim = p.causal ? min(Sk, last + off + 1) : Sk;
-      n_kv[t] = lim > 0 ? (lim + kBN - 1) / kBN : 0;
-      lim_lo[t] = p.causal ? min(Sk, row0[t] + off + 1) : Sk;
+      int lim = Sk, first_lim = Sk;
+      if (p.causal) {
+        lim = min(lim, last + off + 1);
+        first_lim = min(first_lim, row0[t] + off + 1);
+      }
+      if (win_right >= 0) {
+        lim = min_sum(lim, last + off + 1, win_right);
+        first_lim = min_sum(first_lim, row0[t] + off + 1, win_right);
+      }
+      int lo_first = 0;
+      if (win_left >= 0) {
+        lo_first = max(0, row0[t] + off - win_left);
+        lo_hi[t] = max(0, last + off - win_left);
+      }
+      n_kv[t] = lim > lo_first ? (lim + kBN - 1) / kBN : 0;
+      jb[t] = lo_first / kBN;
+      lim_lo[t] = first_lim;
     }
   }
-  const int n_kv_max = max(n_kv[0], n_kv[1]);
+  // Both tiles walk the key tiles [j0, n_kv[t]) with j0 the earlier start:
+  // the later-starting tile (a higher row block) sees its first tiles fully
+  // masked.  cnt[t] = key tiles of tile t, counted from j0.
+  const int j0 = !FEAT ? 0 : n_kv[0] > 0 ? (n_kv[1] > 0 ? min(jb[0], jb[1]) : jb[0]) : (n_kv[1] > 0 ? jb[1] : 0);
+  int cnt[2];
+#pragma unroll
+  for (int t = 0; t < 2; ++t) cnt[t] = n_kv[t] > 0 ? n_kv[t] - j0 : 0;
+  const int n_kv_max = max(cnt[0], cnt[1]);
   const int group = p.num_q_heads / p.num_kv_heads;
   const int kvh = head[0] / group;
 
@@ -197,7 +236,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
 #pragma unroll
       for (int s = 0; s < L::kStages; ++s) filled[s] = 0;
       for (int i = 0; i < 2 * n_kv_max; ++i) {
-        const int j = i >> 1;
+        const int j = j0 + (i >> 1);
         const int s = i % L::kStages;
         const int u = i / L::kStages;
         if (u > 0 && !mbar_wait(bar_kv_empty + 8u * s, (u - 1) & 1, abort_flag, p.wait_limit_ns)) break;
@@ -258,7 +297,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         umma_ts(tmem + L::o_col(t), tmem + L::s_col(t) + kk * 8, b + (uint64_t)((kk * 16 * 128) >> 4),
                 idesc_pv, (acc || kk > 0) ? 1u : 0u);
     };
-    const int nk0 = n_kv[0], nk1 = n_kv[1];
+    const int nk0 = cnt[0], nk1 = cnt[1];
     bool ok = true;
     if (nk0 > 0) ok = mbar_wait(bar_q_full, 0, abort_flag, p.wait_limit_ns);
     if (ok && nk1 > 0) ok = mbar_wait(bar_q_full + 8u, 0, abort_flag, p.wait_limit_ns);
@@ -283,10 +322,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       const int sv = iv % L::kStages;
       if (!mbar_wait(bar_kv_full + 8u * sv, (iv / L::kStages) & 1, abort_flag, p.wait_limit_ns)) break;
       tc_fence_after();
-      if ((j + 1) * kBN > Sk) {
+      if ((j0 + j + 1) * kBN > Sk) {
         // keys at or past kv_len in the last tile: their V rows may hold
         // anything (NaN included); P is 0 there but 0 * NaN is not, so zero them.
-        const int r0 = Sk - j * kBN;
+        const int r0 = Sk - (j0 + j) * kBN;
         uint8_t* vt = smem + (sRing - base) + sv * L::kTileBytes;
         for (int idx = 0; idx < (kBN - r0) * L::kHalves * 8; ++idx) {
           const int chunk = idx & 7;
@@ -343,33 +382,40 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     // put them in local memory)
     const int t_row0 = t ? row0[1] : row0[0];
     const int t_rows = t ? rows[1] : rows[0];
-    const int t_nkv = t ? n_kv[1] : n_kv[0];
+    const int t_nkv = t ? cnt[1] : cnt[0];
     const int t_limlo = t ? lim_lo[1] : lim_lo[0];
+    const int t_lohi = t ? lo_hi[1] : lo_hi[0];
     const int t_head = t ? head[1] : head[0];
     const int r = wq * 32 + lane;
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
     const uint32_t tS = tmem + lane_off + L::s_col(t);
     const uint32_t tO = tmem + lane_off + L::o_col(t);
     const int i_row = t_row0 + r;
-    const int key_lim = p.causal ? min(Sk, i_row + off + 1) : Sk;
+    int key_lim = p.causal ? min(Sk, i_row + off + 1) : Sk;
+    if (win_right >= 0) key_lim = min_sum(key_lim, i_row + off + 1, win_right);
+    const int key_lo = win_left >= 0 ? i_row + off - win_left : 0;
     const float sl2 = p.scale_log2;
+    const float slope = FEAT && p.alibi ? p.alibi[t_head] : 0.f;
     float m = -INFINITY, l = 0.f;
     bool ok = true;
-    for (int j = 0; j < t_nkv; ++j) {
-      if (!mbar_wait(bar_s_full + 8u * t, j & 1, abort_flag, p.wait_limit_ns)) { ok = false; break; }
+    for (int jr = 0; jr < t_nkv; ++jr) {
+      const int j = j0 + jr;                 // key tile
+      if (!mbar_wait(bar_s_full + 8u * t, jr & 1, abort_flag, p.wait_limit_ns)) { ok = false; break; }
       tc_fence_after();
       uint32_t s[4][32];
 #pragma unroll
       for (int c = 0; c < 4; ++c) tmem_ld32(tS + 32 * c, s[c]);
 #pragma unroll
       for (int c = 0; c < 4; ++c) tmem_ld_wait(s[c]);
-      if ((j + 1) * kBN > t_limlo) {
+      if (FEAT && p.score_xform) rewrite_scores(s, p.scale, p.softcap, slope, (float)(i_row + off - j * kBN));
+      if ((j + 1) * kBN > t_limlo || (FEAT && j * kBN < t_lohi)) {
         const int cl = key_lim - j * kBN;  // columns >= cl are masked for this row
+        const int cf = key_lo - j * kBN;   // and columns < cf
 #pragma unroll
         for (int c = 0; c < 4; ++c)
 #pragma unroll
           for (int e = 0; e < 32; ++e)
-            if (32 * c + e >= cl) s[c][e] = 0xFF800000u;  // -inf
+            if (32 * c + e >= cl || (FEAT && 32 * c + e < cf)) s[c][e] = 0xFF800000u;  // -inf
       }
       // row max over the tile's 128 scores: four independent chains of
       // three-input maxima (one per 32-column chunk), then one merge
@@ -409,7 +455,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         }
         tmem_st16(tS + 16 * c, pk);
       }
-      if (j > 0 && __any_sync(0xFFFFFFFFu, alpha != 1.f)) {
+      if (jr > 0 && __any_sync(0xFFFFFFFFu, alpha != 1.f)) {
         // O_t is final for tile j-1 here: S_t(j) was issued after PV_t(j-1)
         // and its commit covers every earlier MMA.
         const float2 a2 = make_float2(alpha, alpha);
@@ -440,7 +486,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     }
     const bool row_ok = r < t_rows;
     const int64_t tok = (int64_t)q_begin + t_row0 + r;
-    const float inv_l = l > 0.f ? 1.f / l : 0.f;
+    float inv_l, lse_v;
+    finish_row(m, l, FEAT && p.sinks ? p.sinks[t_head] : -INFINITY, inv_l, lse_v);
     if (t_rows == kBM && p.rounding != 3) {
       // Full tile, 16-bit output: the rows are written into this tile's Q
       // slot (free: the o_full commit covers every product that read it) in
@@ -553,7 +600,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       // packed: [total_q, Hq]; dense: [batch, Hq, Sq]
       const int64_t li = p.dense ? ((int64_t)b * p.num_q_heads + t_head) * Sq + t_row0 + r
                                  : tok * p.num_q_heads + t_head;
-      p.lse[li] = l > 0.f ? m * kLn2 + logf(l) : -INFINITY;
+      p.lse[li] = lse_v;
     }
   }
 
@@ -566,14 +613,20 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
   if (threadIdx.x == 0 && *abort_flag) report_status(p.status, kStatusTimeout);
 }
 
-template <int D, bool BF16>
-cudaError_t launch_one(const PrefillParams& p, dim3 grid, cudaStream_t stream) {
+template <int D, bool BF16, bool FEAT>
+cudaError_t launch_one_f(const PrefillParams& p, dim3 grid, cudaStream_t stream) {
   using L = PrefillLayout<D>;
   static std::atomic<uint64_t> smem_set{0};
-  const cudaError_t e = ensure_dynamic_smem(prefill_kernel<D, BF16>, L::kSmemBytes, smem_set);
+  const cudaError_t e = ensure_dynamic_smem(prefill_kernel<D, BF16, FEAT>, L::kSmemBytes, smem_set);
   if (e != cudaSuccess) return e;
-  prefill_kernel<D, BF16><<<grid, kThreads, L::kSmemBytes, stream>>>(p);
+  prefill_kernel<D, BF16, FEAT><<<grid, kThreads, L::kSmemBytes, stream>>>(p);
   return cudaGetLastError();
+}
+
+template <int D, bool BF16>
+cudaError_t launch_one(const PrefillParams& p, dim3 grid, cudaStream_t stream) {
+  const bool feat = p.win_left >= 0 || p.win_right >= 0 || p.score_xform || p.sinks;
+  return feat ? launch_one_f<D, BF16, true>(p, grid, stream) : launch_one_f<D, BF16, false>(p, grid, stream);
 }
 
 }  // namespace

@@ -4,9 +4,9 @@ The dispatcher of "gfx942 unified attention, from the math up" (sec. 9)
 replays decode steps and short prefills from a captured graph and runs long
 prefills eagerly: a decode step (one query row per sequence) or a prefill of
 at most 768 query rows is dominated by launch and host time, a long prefill
-is not.  Feature-flagged variants are never graphed there; this library has
-none.  A call made while the caller's stream is already being captured is
-simply recorded into the caller's graph instead.
+is not.  Feature-flagged calls (sliding window, softcap, ALiBi, sinks) are
+never graphed, as there.  A call made while the caller's stream is already
+being captured is simply recorded into the caller's graph instead.
 
 A graph bakes in every pointer, size and scalar of the call it recorded, so
 the cache is keyed on all of them: replaying a key runs the same kernels on
@@ -17,15 +17,16 @@ from __future__ import annotations
 
 import torch
 
-from . import attn_decode_workspace_size, attn_fwd_decode, attn_fwd_prefill
+from . import attn_decode_workspace_size, attn_fwd_decode, attn_fwd_prefill, has_features
 
 GRAPH_MAX_SEQLEN_Q = 768   # the pages' threshold: graph at or below, eager above
 
 
-def should_graph(max_seqlen_q: int) -> bool:
+def should_graph(max_seqlen_q: int, featured: bool = False) -> bool:
     """The replay policy: decode (max_seqlen_q == 1) and short prefill
-    (max_seqlen_q <= 768) are graphed; longer prefill is not."""
-    return 1 <= int(max_seqlen_q) <= GRAPH_MAX_SEQLEN_Q
+    (max_seqlen_q <= 768) are graphed; longer prefill and feature-flagged
+    calls are not."""
+    return not featured and 1 <= int(max_seqlen_q) <= GRAPH_MAX_SEQLEN_Q
 
 
 def _key(name, tensors, scalars):
@@ -90,12 +91,21 @@ def default_cache() -> GraphCache:
 
 
 def decode(out, q, k_cache, v_cache, block_table, seq_lens, *, max_seqlen_k: int, scale: float,
-           num_splits: int, workspace, rounding: int = 0, lse=None, cache: GraphCache | None = None):
-    """attn_fwd_decode through the replay cache (decode is always graphed).
-    The workspace must be supplied (a graph cannot allocate)."""
+           num_splits: int, workspace, rounding: int = 0, lse=None, cache: GraphCache | None = None,
+           **features) -> bool:
+    """attn_fwd_decode through the replay cache (decode is graphed unless it
+    carries feature flags, which run eagerly).  The workspace must be
+    supplied (a graph cannot allocate).  Returns True when the call went
+    through the cache."""
     if workspace is None:
         raise ValueError("graphed decode needs a caller workspace of "
                          "attn_decode_workspace_size(...) bytes")
+    if not should_graph(1, has_features(**features)):
+        attn_fwd_decode(out, q, k_cache, v_cache, block_table, seq_lens,
+                        max_seqlen_k=max_seqlen_k, scale=scale, num_splits=num_splits,
+                        workspace=workspace, rounding=rounding, lse=lse,
+                        stream=torch.cuda.current_stream(), **features)
+        return False
     cache = _default if cache is None else cache
     tensors = (out, q, k_cache, v_cache, block_table, seq_lens, workspace, lse)
     key = _key("decode", tensors, (int(max_seqlen_k), float(scale), int(num_splits),
@@ -107,19 +117,20 @@ def decode(out, q, k_cache, v_cache, block_table, seq_lens, *, max_seqlen_k: int
                         workspace=workspace, rounding=rounding, lse=lse, stream=stream)
 
     cache.run(key, tensors, fn)
+    return True
 
 
 def prefill(out, q, k_cache, v_cache, block_table, query_start_loc, seq_lens, *,
             max_seqlen_q: int, max_seqlen_k: int, scale: float, causal: bool, rounding: int = 0,
-            lse=None, cache: GraphCache | None = None) -> bool:
+            lse=None, cache: GraphCache | None = None, **features) -> bool:
     """attn_fwd_prefill, replayed from a graph when the policy says so.
     Returns True when the call went through the cache."""
     def fn(stream):
         attn_fwd_prefill(out, q, k_cache, v_cache, block_table, query_start_loc, seq_lens,
                          max_seqlen_q=max_seqlen_q, max_seqlen_k=max_seqlen_k, scale=scale,
-                         causal=causal, rounding=rounding, lse=lse, stream=stream)
+                         causal=causal, rounding=rounding, lse=lse, stream=stream, **features)
 
-    if not should_graph(max_seqlen_q):
+    if not should_graph(max_seqlen_q, has_features(**features)):
         fn(torch.cuda.current_stream())
         return False
     cache = _default if cache is None else cache

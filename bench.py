@@ -73,28 +73,62 @@ MEASURED_TRAFFIC = {
 # algorithmic work
 # ----------------------------------------------------------------------------
 
-def visible_pairs(q_lens, kv_lens, causal: bool) -> int:
+def visible_pairs(q_lens, kv_lens, causal: bool, window=(-1, -1)) -> int:
     """(query row, key) pairs left visible by the mask, per query head;
-    bottom-right causal alignment: row i of a sequence sees j <= i + Sk - Sq."""
+    bottom-right causal alignment: row i of a sequence sees j <= i + Sk - Sq,
+    a sliding window (left, right) keeps diag - left <= j <= diag + right."""
     tot = 0
     for sq, sk in zip(q_lens, kv_lens):
-        if not causal:
-            tot += sq * sk
-            continue
-        off = sk - sq
-        i = np.arange(sq, dtype=np.int64)
-        tot += int(np.clip(np.minimum(sk, i + off + 1), 0, None).sum())
+        diag = np.arange(sq, dtype=np.int64) + (sk - sq)
+        hi = np.full(sq, sk, dtype=np.int64)                 # exclusive upper bound
+        if causal:
+            hi = np.minimum(hi, diag + 1)
+        if window[1] >= 0:
+            hi = np.minimum(hi, diag + window[1] + 1)
+        lo = np.zeros(sq, dtype=np.int64)
+        if window[0] >= 0:
+            lo = np.maximum(lo, diag - window[0])
+        tot += int(np.clip(hi - lo, 0, None).sum())
     return tot
 
 
-def prefill_flops(prob) -> float:
+def prefill_flops(prob, window=(-1, -1)) -> float:
     return 4.0 * prob.head_size * prob.num_q_heads * visible_pairs(prob.q_lens, prob.kv_lens,
-                                                                   prob.causal)
+                                                                   prob.causal, window)
 
 
-def decode_bytes(prob) -> float:
+# Feature-flagged sweep workloads: (base workload, flags).  The per-head
+# arrays are built on the device from these recipes.
+FEATURE_WORKLOADS = {
+    "prefill_causal_bf16_s8192_window1024": ("prefill_causal_bf16_s8192", {"window": (1024, -1)}),
+    "prefill_causal_bf16_s8192_softcap": ("prefill_causal_bf16_s8192", {"softcap": 30.0}),
+    "prefill_causal_bf16_s8192_alibi_sinks": ("prefill_causal_bf16_s8192",
+                                              {"alibi": True, "sinks": True}),
+    "decode_bf16_b64_paged16_window1024": ("decode_bf16_b64_paged16", {"window": (1024, -1)}),
+}
+
+
+def feature_args(recipe: dict, num_q_heads: int, dev) -> dict:
+    out = {}
+    if "window" in recipe:
+        out["window"] = recipe["window"]
+    if "softcap" in recipe:
+        out["softcap"] = recipe["softcap"]
+    if recipe.get("alibi"):
+        out["alibi_slopes"] = torch.tensor([2.0 ** (-8.0 * (h + 1) / num_q_heads)
+                                            for h in range(num_q_heads)],
+                                           dtype=torch.float32, device=dev)
+    if recipe.get("sinks"):
+        out["sinks"] = torch.zeros(num_q_heads, dtype=torch.float32, device=dev)
+    return out
+
+
+def decode_bytes(prob, window=(-1, -1)) -> float:
+    """K + V bytes of the visible keys (a left window keeps the last
+    left + 1 keys of each sequence) plus Q and O."""
     el = 2
-    kv = 2.0 * sum(prob.kv_lens) * prob.num_kv_heads * prob.head_size * el
+    keys = [min(k, window[0] + 1) if window[0] >= 0 else k for k in prob.kv_lens]
+    kv = 2.0 * sum(keys) * prob.num_kv_heads * prob.head_size * el
     qo = 2.0 * prob.num_seqs * prob.num_q_heads * prob.head_size * el
     return kv + qo
 
@@ -560,9 +594,13 @@ def run_sweep(args, dev):
     peaks, peak_src = load_peaks()
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
-    names = args.sweep.split(",") if args.sweep != "all" else list(attn_inputs.WORKLOADS)
+    names = (args.sweep.split(",") if args.sweep != "all"
+             else list(attn_inputs.WORKLOADS) + list(FEATURE_WORKLOADS))
     for name in names:
-        prob = attn_inputs.workload(name)
+        base, recipe = FEATURE_WORKLOADS.get(name, (name, {}))
+        prob = attn_inputs.workload(base)
+        feat = feature_args(recipe, prob.num_q_heads, dev)
+        window = recipe.get("window", (-1, -1))
         t = device_args(prob, dev)
         out = torch.empty_like(t["q"])
         is_decode = prob.max_seqlen_q == 1
@@ -575,14 +613,14 @@ def run_sweep(args, dev):
                 attn.attn_fwd_decode(out, t["q"], t["k_cache"], t["v_cache"], t["block_table"],
                                      t["seq_lens"], max_seqlen_k=prob.max_seqlen_k,
                                      scale=prob.scale, num_splits=DECODE_SPLITS, workspace=ws,
-                                     stream=stream)
+                                     stream=stream, **feat)
         else:
             def call():
                 attn.attn_fwd_prefill(out, t["q"], t["k_cache"], t["v_cache"], t["block_table"],
                                       t["query_start_loc"], t["seq_lens"],
                                       max_seqlen_q=prob.max_seqlen_q,
                                       max_seqlen_k=prob.max_seqlen_k, scale=prob.scale,
-                                      causal=prob.causal, stream=stream)
+                                      causal=prob.causal, stream=stream, **feat)
         for _ in range(args.warmup):
             flush.zero_()
             call()
@@ -605,9 +643,10 @@ def run_sweep(args, dev):
         sampler.stop()
         us = statistics.median(a.elapsed_time(b) for a, b in evs) * 1e3
         if is_decode:
-            value, unit, peak = decode_bytes(prob) / us / 1e3, "GB/s", peaks["hbm_gbs"]
+            value, unit, peak = decode_bytes(prob, window) / us / 1e3, "GB/s", peaks["hbm_gbs"]
         else:
-            value, unit, peak = prefill_flops(prob) / us / 1e6, "TFLOP/s", peaks["bf16_tflops"]
+            value, unit, peak = (prefill_flops(prob, window) / us / 1e6, "TFLOP/s",
+                                 peaks["bf16_tflops"])
         print(json.dumps({"workload": name, "us": us, "value": value, "unit": unit,
                           "frac": value / peak, "peak": peak, "peak_source": peak_src,
                           "calls": n, "clocks": sampler.summary(t0, t1)}), flush=True)

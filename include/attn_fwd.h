@@ -200,6 +200,71 @@ attn_status_t attn_fwd_decode(void* out, const void* q, const void* k_cache, con
                               float* lse_out, void* workspace, size_t workspace_bytes,
                               int32_t* status_dev, void* stream);
 
+/*
+ * Feature-flagged variants.  "gfx942 unified attention, from the math up",
+ * sec. 9, names sinks, ALiBi, softcap and sliding window among the flags a
+ * dispatcher treats specially (it keeps such calls out of graph replay)
+ * without defining them; this library takes their usual definitions.  With
+ * diag = i + kv_len - query_len the key aligned with query row i (for decode
+ * diag = kv_len - 1) and s = scale * q.k the scaled score:
+ *   window_left  >= 0: key j is visible only if j >= diag - window_left;
+ *                -1: unbounded.  Key tiles wholly left of every row's window
+ *                are skipped, not computed and masked.
+ *   window_right >= 0: key j is visible only if j <= diag + window_right;
+ *                -1: unbounded (causal calls are already bounded by diag).
+ *   softcap      > 0: s becomes softcap * tanh(s / softcap); 0: off.
+ *   alibi_slopes NULL, or a DEVICE fp32 array [num_q_heads]: s gains
+ *                -alibi_slopes[h] * |diag - j| (after the softcap).
+ *   sinks        NULL, or a DEVICE fp32 array [num_q_heads]: a logit z_h that
+ *                joins the softmax denominator with no value row,
+ *                O = sum_j e^(s_j) V_j / (sum_j e^(s_j) + e^(z_h)); the
+ *                log-sum-exp output includes it (z_h for a row with no
+ *                visible key, whose output is 0).
+ * Passing NULL for the whole struct, or {-1, -1, 0, NULL, NULL}, is the plain
+ * call.  Errors: window values below -1, a softcap that is negative or not
+ * finite, or per-head arrays that are not 4-byte aligned give
+ * ATTN_ERR_INVALID_ARG.  The struct is read during the call only; the
+ * device arrays must stay valid until the work on `stream` has run.
+ */
+typedef struct {
+  int32_t window_left;
+  int32_t window_right;
+  float softcap;
+  const float* alibi_slopes;
+  const float* sinks;
+} attn_features_t;
+
+/* attn_fwd_prefill, attn_fwd_dense and attn_fwd_decode with feature flags
+ * (the other arguments as for those calls).  Decode with any feature runs
+ * the SIMT split kernel. */
+attn_status_t attn_fwd_prefill_ex(void* out, const void* q, const void* k_cache,
+                                  const void* v_cache, const int32_t* block_table,
+                                  int32_t block_table_stride, const int32_t* query_start_loc,
+                                  const int32_t* seq_lens, int32_t num_seqs, int32_t max_seqlen_q,
+                                  int32_t max_seqlen_k, int32_t total_q, int32_t num_q_heads,
+                                  int32_t num_kv_heads, int32_t head_size, int32_t block_size,
+                                  int32_t num_blocks, float scale, int32_t causal,
+                                  attn_dtype_t dtype, attn_round_t rounding, float* lse_out,
+                                  int32_t* status_dev, void* stream,
+                                  const attn_features_t* features);
+attn_status_t attn_fwd_dense_ex(void* out, const void* q, const void* k, const void* v,
+                                const int64_t* q_strides, const int64_t* k_strides,
+                                const int64_t* v_strides, const int64_t* o_strides, int32_t batch,
+                                int32_t seqlen_q, int32_t seqlen_k, int32_t num_q_heads,
+                                int32_t num_kv_heads, int32_t head_size, float scale,
+                                int32_t causal, attn_dtype_t dtype, attn_round_t rounding,
+                                float* lse_out, int32_t* status_dev, void* stream,
+                                const attn_features_t* features);
+attn_status_t attn_fwd_decode_ex(void* out, const void* q, const void* k_cache,
+                                 const void* v_cache, const int32_t* block_table,
+                                 int32_t block_table_stride, const int32_t* seq_lens,
+                                 int32_t num_seqs, int32_t max_seqlen_k, int32_t num_q_heads,
+                                 int32_t num_kv_heads, int32_t head_size, int32_t block_size,
+                                 int32_t num_blocks, float scale, int32_t num_splits,
+                                 attn_dtype_t dtype, attn_round_t rounding, float* lse_out,
+                                 void* workspace, size_t workspace_bytes, int32_t* status_dev,
+                                 void* stream, const attn_features_t* features);
+
 /* Size of the device scratch array built into the library for
  * attn_fwd_decode_noalloc (16 MiB on every GPU that loads the library). */
 #define ATTN_DECODE_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)

@@ -24,12 +24,14 @@ def gpu_prefill(prob, t=None, rounding=0, lse=False, status=None):
                         rounding=rounding, return_lse=lse, status=status)
 
 
-def gpu_decode(prob, t=None, splits=8, rounding=0, lse=False, status=None, workspace=None):
+def gpu_decode(prob, t=None, splits=8, rounding=0, lse=False, status=None, workspace=None,
+               **features):
     import attention_forward_sdpa_gb300 as attn
     t = t or to_dev(prob)
     return attn.decode(t["q"], t["k_cache"], t["v_cache"], t["block_table"], t["seq_lens"],
                        max_seqlen_k=prob.max_seqlen_k, scale=prob.scale, num_splits=splits,
-                       rounding=rounding, return_lse=lse, status=status, workspace=workspace)
+                       rounding=rounding, return_lse=lse, status=status, workspace=workspace,
+                       **features)
 
 
 def oracle_run(prob, rows=None, threads=None):

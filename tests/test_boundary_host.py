@@ -190,6 +190,46 @@ def test_timeout_hook_rejects_bad_arguments(lib):
     assert lib.attn_test_prefill_timeout(*a, status, 5_000_000_000, stream) == 1   # limit > 4 s
 
 
+class Feat(ctypes.Structure):
+    _fields_ = [("window_left", ctypes.c_int32), ("window_right", ctypes.c_int32),
+                ("softcap", ctypes.c_float), ("alibi_slopes", ctypes.c_void_p),
+                ("sinks", ctypes.c_void_p)]
+
+
+@pytest.mark.parametrize("feat", [
+    Feat(-2, -1, 0.0, None, None),                 # window below -1
+    Feat(-1, -5, 0.0, None, None),
+    Feat(-1, -1, -1.0, None, None),                # negative softcap
+    Feat(-1, -1, float("nan"), None, None),
+    Feat(-1, -1, float("inf"), None, None),
+    Feat(-1, -1, 0.0, 0x10002, None),              # misaligned per-head arrays
+    Feat(-1, -1, 0.0, None, 0x10001),
+])
+def test_feature_flags_are_validated(lib, feat):
+    import attention_forward_sdpa_gb300 as pkg
+    pkg.load_library()                             # sets the _ex argtypes
+    P = ctypes.POINTER(pkg._Features)
+    f = pkg._Features(feat.window_left, feat.window_right, feat.softcap, feat.alibi_slopes,
+                      feat.sinks)
+    assert lib.attn_fwd_prefill_ex(*prefill_args(), ctypes.cast(ctypes.byref(f), P)) == 1
+    assert lib.attn_fwd_decode_ex(*decode_args(), ctypes.cast(ctypes.byref(f), P)) == 1
+    qs = (ctypes.c_int64 * 3)(4096, 1024, 128)
+    assert lib.attn_fwd_dense_ex(FAKE, FAKE, FAKE, FAKE, qs, qs, qs, qs, 2, 32, 16, 8, 2, 128,
+                                 0.088, 1, 1, 0, None, None, None,
+                                 ctypes.cast(ctypes.byref(f), P)) == 1
+
+
+def test_valid_feature_flags_pass_validation(lib):
+    """Valid flags on an empty problem: the call is a no-op that returns OK
+    without touching a GPU."""
+    import attention_forward_sdpa_gb300 as pkg
+    pkg.load_library()
+    f = pkg._Features(128, 0, 30.0, None, None)
+    P = ctypes.POINTER(pkg._Features)
+    assert lib.attn_fwd_prefill_ex(*prefill_args(num_seqs=0), ctypes.cast(ctypes.byref(f), P)) == 0
+    assert lib.attn_fwd_prefill_ex(*prefill_args(num_seqs=0), None) == 0
+
+
 def test_round_rejects_bad_arguments(lib):
     assert lib.attn_round_f32(FAKE, FAKE, -1, 1, 0, None) == 1
     assert lib.attn_round_f32(FAKE, FAKE, 10, 1, 3, None) == 1

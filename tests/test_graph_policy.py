@@ -1,9 +1,11 @@
 """The graph-replay policy of "gfx942 unified attention, from the math up",
 sec. 9 (host logic, no GPU): decode and prefill of at most 768 query rows are
-graphed, longer prefill is not; and the cache key changes with every pointer,
-shape and scalar that a recorded graph would bake in."""
+graphed, longer prefill and feature-flagged calls are not; and the cache key
+changes with every pointer, shape and scalar that a recorded graph would bake
+in."""
 import torch
 
+import attention_forward_sdpa_gb300 as attn
 from attention_forward_sdpa_gb300 import graphs
 
 
@@ -14,6 +16,16 @@ def test_policy_thresholds():
     assert not graphs.should_graph(769)
     assert not graphs.should_graph(8192)
     assert not graphs.should_graph(0)      # nothing to run
+
+
+def test_feature_flagged_calls_are_not_graphed():
+    assert not graphs.should_graph(1, True)
+    assert not graphs.should_graph(128, True)
+    assert not attn.has_features()
+    assert attn.has_features(window=(128, -1))
+    assert attn.has_features(softcap=30.0)
+    assert attn.has_features(alibi_slopes=torch.zeros(4))
+    assert attn.has_features(sinks=torch.zeros(4))
 
 
 def test_cache_key_sees_pointers_shapes_and_scalars():
