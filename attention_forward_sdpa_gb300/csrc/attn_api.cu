@@ -154,8 +154,7 @@ int decode_prepare_and_launch(DecodeParams& p, int head_size, bool bf16, void* w
   }
   const int G = p.num_q_heads / p.num_kv_heads;
   const bool pow2 = (G & (G - 1)) == 0;
-  const bool features = p.win_left >= 0 || p.score_xform || p.sinks;
-  const bool tc_path = head_size == 128 && ((G <= 16 && pow2) || G % 16 == 0) && !features;
+  const bool tc_path = head_size == 128 && ((G <= 16 && pow2) || G % 16 == 0);
   if (!tc_path) {
     cudaError_t e = launch_decode(p, head_size, bf16, G, stream);
     return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;

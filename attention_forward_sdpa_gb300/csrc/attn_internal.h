@@ -85,8 +85,8 @@ struct DecodeParams {
   int32_t num_splits;
   int32_t rounding;
   float scale_log2;
-  // feature flags, as in PrefillParams (the SIMT split kernel and the merge
-  // honour them; the tcgen05 decode kernel is not used when any is set)
+  // feature flags, as in PrefillParams (both split kernels and the merge
+  // honour them)
   int32_t win_left;
   int32_t score_xform;
   float softcap;

@@ -34,6 +34,7 @@
 
 #include "attn_internal.h"
 #include "round16.cuh"
+#include "score_features.cuh"
 #include "sm103_ptx.cuh"
 
 namespace attn {
@@ -51,6 +52,7 @@ constexpr int kPBytes = 2 * 16 * 128;           // two row halves of [16 heads][
 constexpr int kSeqCache = 2048;                 // cached sequence lengths
 constexpr int kSortMax = 128;                   // longest-first order up to this many sequences
 constexpr float kLn2 = 0.693147180559945309f;
+constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleSlack = 8.f;            // log2 units
 
 struct ItemEntry {
@@ -59,7 +61,8 @@ struct ItemEntry {
   int q0;      // first query head of the item (column 0)
   int split;
   int k0, k1;  // key range
-  int pad[2];
+  int lo;      // first visible key (a sliding window masks the keys below)
+  int sk;      // the sequence's KV length (its decode row is aligned with key sk - 1)
 };
 
 constexpr int kRingOff = 0;
@@ -232,7 +235,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
       if (lane == 0) item = atomicAdd(p.counter, 1);
       item = __shfl_sync(0xFFFFFFFFu, item, 0);
       const bool end = item >= p.n_items;
-      int b = -1, kvh0 = 0, q0 = 0, split = 0, k0 = 0, k1 = 0;
+      int b = -1, kvh0 = 0, q0 = 0, split = 0, k0 = 0, k1 = 0, lo = 0, sk = 0;
       if (!end) {
         split = item % p.num_splits;
         const int rest = item / p.num_splits;
@@ -246,7 +249,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
           if (lane == 0) report_status(p.status, kStatusBadArg);
           Sk = 0;
         }
-        split_keys(Sk, p.num_splits, split, k0, k1);
+        // a sliding window keeps keys >= lo: the splits cut [lo rounded
+        // down to 16, Sk), so boxes stay page-aligned, and the softmax masks
+        // the keys below lo
+        if (p.win_left >= 0) lo = max(0, Sk - 1 - p.win_left);
+        sk = Sk;
+        const int lo16 = lo & ~15;
+        split_keys(Sk - lo16, p.num_splits, split, k0, k1);
+        k0 += lo16;
+        k1 += lo16;
       }
       const uint32_t rs = seen % kItemRing;
       if (seen >= kItemRing &&
@@ -255,7 +266,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
       if (lane == 0) {
         ItemEntry e;
         e.b = b; e.kvh0 = kvh0; e.q0 = q0; e.split = split; e.k0 = k0; e.k1 = k1;
-        e.pad[0] = e.pad[1] = 0;
+        e.lo = lo; e.sk = sk;
         items[rs] = e;
         mbar_arrive(bar_item_full + 8u * rs);
       }
@@ -419,6 +430,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
     const int cwin = F >= 2 ? ((2 * quarter) % F) * GH : 0;
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     const float sl2 = p.scale_log2;
+    const float inv_cap = p.softcap > 0.f ? 1.f / p.softcap : 0.f;
     const int Hq = p.num_q_heads;
     uint32_t seen = 0, g = 0, red_uses = 0;
     bool ok = true;
@@ -437,6 +449,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
       ++seen;
       if (e.b < 0) break;
       const int n_tiles = (e.k1 - e.k0 + KT - 1) / KT;
+      // query head of the row's column j is qbase + j
+      const int qbase = (e.kvh0 + hrow) * G + (e.q0 - e.kvh0 * G);
+      float slope[GH];
+#pragma unroll
+      for (int j = 0; j < GH; ++j) slope[j] = p.alibi ? p.alibi[qbase + j] : 0.f;
       float mcol[16];   // running max of every column (kept identically by all threads)
 #pragma unroll
       for (int c = 0; c < 16; ++c) mcol[c] = -INFINITY;
@@ -456,14 +473,23 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
         uint32_t sv[SW];
         tmem_ld_n<SW>(tmem + lane_off + s_col(g) + cwin, sv);
         tmem_ld_wait_n<SW>(sv);
-        const bool valid = e.k0 + t * KT + krow < e.k1;
+        const int key = e.k0 + t * KT + krow;
+        const bool valid = key >= e.lo && key < e.k1;
         const bool upper = SW > GH && F >= 2 && lane >= 16;
         float x[GH];
         bool raise = false;
 #pragma unroll
         for (int j = 0; j < GH; ++j) {
           const float v = __uint_as_float(upper ? sv[(GH + j) % SW] : sv[j]);
-          x[j] = valid ? v * sl2 : -INFINITY;
+          if (p.score_xform) {
+            // softcap, then ALiBi on the scaled score; distance to the
+            // decode row's aligned key
+            const float xs = rewrite_score(v * p.scale, p.softcap, inv_cap, slope[j],
+                                           (float)(e.sk - 1 - key));
+            x[j] = valid ? xs * kLog2e : -INFINITY;
+          } else {
+            x[j] = valid ? v * sl2 : -INFINITY;
+          }
           raise |= x[j] > m[j] + kRescaleSlack;
         }
         // Announce before the exchange whether any score of this tile exceeds
@@ -606,10 +632,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
             p.part_ml[(row * p.num_splits + e.split) * 2 + 1] = L;
           }
         } else {
-          const float v = L > 0.f ? o[c] / L : 0.f;
+          // one split: normalise here, with the sink logit in the
+          // denominator when the call has one
+          float inv_l, lse_v;
+          finish_row(mcol[c], L, p.sinks ? p.sinks[qh] : -INFINITY, inv_l, lse_v);
+          const float v = o[c] * inv_l;
           if (p.rounding == 3) static_cast<float*>(p.out)[row * kD + r] = v;
           else static_cast<uint16_t*>(p.out)[row * kD + r] = round_out<BF16>(v, p.rounding);
-          if (r == 0 && p.lse) p.lse[row] = L > 0.f ? mcol[c] * kLn2 + logf(L) : -INFINITY;
+          if (r == 0 && p.lse) p.lse[row] = lse_v;
         }
       }
     }

@@ -1,5 +1,5 @@
 // score_features.cuh -- the feature-flagged score rewrites and the sink term
-// shared by the prefill kernels and the SIMT decode kernel ("gfx942 unified
+// shared by the prefill kernels and both decode kernels ("gfx942 unified
 // attention, from the math up", sec. 9 names softcap, ALiBi and sinks; the
 // definitions are the usual ones, stated in include/attn_fwd.h).
 #pragma once
@@ -10,20 +10,13 @@
 
 namespace attn {
 
-// tanh(y) = 1 - 2 / (e^(2y) + 1), from the exponential (an identity, not a
-// library routine).  |y| is clamped to 10, where tanh is +-1 to within fp32
-// rounding, so that e^(2y) stays finite.  Absolute error ~1e-7, which is
-// what matters for a capped logit.
-__device__ __forceinline__ float tanh_via_exp2(float y) {
-  const float yc = fminf(fmaxf(y, -10.f), 10.f);
-  const float e = fast_exp2(yc * 2.8853900817779268f);   // 2 * log2(e)
-  return 1.f - __fdividef(2.f, e + 1.f);
-}
-
 // One scaled score x = tau * q.k: softcap, then the ALiBi bias -slope * dist.
+// The cap uses the MUFU tanh: its relative error (about 2^-11) moves a capped
+// score y by at most |y| * 2^-11 (< cap * 2^-11), so each probability moves by
+// that relative amount, a fifth of the 2^-9 relative step of a bf16 output.
 __device__ __forceinline__ float rewrite_score(float x, float cap, float inv_cap, float slope,
                                                float dist) {
-  if (cap > 0.f) x = cap * tanh_via_exp2(x * inv_cap);
+  if (cap > 0.f) x = cap * fast_tanh(x * inv_cap);
   return fmaf(-slope, fabsf(dist), x);
 }
 
@@ -31,17 +24,29 @@ __device__ __forceinline__ float rewrite_score(float x, float cap, float inv_cap
 // 32c + e): each becomes (rewrite(tau * q.k)) / tau, so that the softmax that
 // follows, which multiplies by tau * log2(e), sees the rewritten score.  d0 is
 // the distance from the row's aligned key to column 0 (diag - first key).
+// The constants are folded so that an element costs one multiply, one MUFU
+// tanh and one FMA: (cap / tau) * tanh(q.k * tau / cap) - (slope / tau) * |dist|.
 __device__ __forceinline__ void rewrite_scores(uint32_t (&s)[4][32], float tau, float cap,
                                                float slope, float d0) {
   const float inv_tau = 1.f / tau;
-  const float inv_cap = cap > 0.f ? 1.f / cap : 0.f;
+  const float ks = -slope * inv_tau;
+  if (cap > 0.f) {
+    const float a = tau / cap;
+    const float b = cap * inv_tau;
 #pragma unroll
-  for (int c = 0; c < 4; ++c)
+    for (int c = 0; c < 4; ++c)
 #pragma unroll
-    for (int e = 0; e < 32; ++e) {
-      const float x = __uint_as_float(s[c][e]) * tau;
-      s[c][e] = __float_as_uint(rewrite_score(x, cap, inv_cap, slope, d0 - (float)(32 * c + e)) * inv_tau);
-    }
+      for (int e = 0; e < 32; ++e) {
+        const float t = fast_tanh(__uint_as_float(s[c][e]) * a);
+        s[c][e] = __float_as_uint(fmaf(ks, fabsf(d0 - (float)(32 * c + e)), t * b));
+      }
+  } else {
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+#pragma unroll
+      for (int e = 0; e < 32; ++e)
+        s[c][e] = __float_as_uint(fmaf(ks, fabsf(d0 - (float)(32 * c + e)), __uint_as_float(s[c][e])));
+  }
 }
 
 // Final normalisation of a row: m is the running reference max (log2 units),

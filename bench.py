@@ -105,6 +105,9 @@ FEATURE_WORKLOADS = {
     "prefill_causal_bf16_s8192_alibi_sinks": ("prefill_causal_bf16_s8192",
                                               {"alibi": True, "sinks": True}),
     "decode_bf16_b64_paged16_window1024": ("decode_bf16_b64_paged16", {"window": (1024, -1)}),
+    "decode_bf16_b64_paged16_softcap_alibi_sinks": ("decode_bf16_b64_paged16",
+                                                    {"softcap": 30.0, "alibi": True,
+                                                     "sinks": True}),
 }
 
 

@@ -235,8 +235,8 @@ typedef struct {
 } attn_features_t;
 
 /* attn_fwd_prefill, attn_fwd_dense and attn_fwd_decode with feature flags
- * (the other arguments as for those calls).  Decode with any feature runs
- * the SIMT split kernel. */
+ * (the other arguments as for those calls).  Decode keeps its kernel choice:
+ * a window only narrows the key range each split reads. */
 attn_status_t attn_fwd_prefill_ex(void* out, const void* q, const void* k_cache,
                                   const void* v_cache, const int32_t* block_table,
                                   int32_t block_table_stride, const int32_t* query_start_loc,

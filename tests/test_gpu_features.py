@@ -1,8 +1,9 @@
 """GPU parity of the feature-flagged variants (sliding window, softcap, ALiBi,
 sinks; named in "gfx942 unified attention, from the math up", sec. 9) against
 the fp64 oracle, for the paged prefill (head sizes 64, 128, 256; GQA pairs of
-heads and row-block pairs), the dense strided entry point, and decode (SIMT
-split kernel plus merge, one and several splits).
+heads and row-block pairs), the dense strided entry point, and decode (the
+tcgen05 split kernel at head size 128, the SIMT one otherwise, plus the merge;
+one and several splits).
 
 Tolerance: 2e-2 (fp16) / 4e-2 (bf16) max |err|, as for the plain calls.  The
 windows are chosen so that whole key tiles fall left of every row of a query
@@ -51,6 +52,8 @@ def features(kind, h, seed):
         return dict(window=(150, 90))
     if kind == "softcap":
         return dict(softcap=4.0)
+    if kind == "softcap_wide":
+        return dict(softcap=30.0)
     if kind == "alibi":
         return dict(alibi_slopes=slopes(h))
     if kind == "sinks":
@@ -61,7 +64,7 @@ def features(kind, h, seed):
     raise KeyError(kind)
 
 
-KINDS = ("window_causal", "window_band", "softcap", "alibi", "sinks", "all")
+KINDS = ("window_causal", "window_band", "softcap", "softcap_wide", "alibi", "sinks", "all")
 SHAPES = {
     # d, Hq, Hkv, dtype, block size
     "d128_gqa4_bf16": (128, 8, 2, torch.bfloat16, 64),
@@ -164,7 +167,7 @@ def test_dense_features_equal_paged(layout):
 
 @pytest.mark.parametrize("splits", [1, 8])
 @pytest.mark.parametrize("kind", ("window_causal", "softcap", "alibi", "sinks", "all"))
-@pytest.mark.parametrize("d,hq,hkv", [(128, 32, 8), (64, 6, 2), (256, 8, 2)])
+@pytest.mark.parametrize("d,hq,hkv", [(128, 32, 8), (128, 16, 2), (64, 6, 2), (256, 8, 2)])
 def test_decode_features(splits, kind, d, hq, hkv):
     prob = attn_inputs.paged_problem(seed=86, q_lens=[1] * 6, kv_lens=[1, 17, 0, 300, 2049, 700],
                                      num_q_heads=hq, num_kv_heads=hkv, head_size=d, block_size=16,
