@@ -55,6 +55,14 @@ class PagedProblem:
     scale: float
     causal: bool
     meta: dict = field(default_factory=dict)
+    # fp8 caches: K and V hold float8_e4m3fn codes and the values meant are
+    # code * k_scale and code * v_scale (1.0 for 16-bit caches)
+    k_scale: float = 1.0
+    v_scale: float = 1.0
+
+    @property
+    def kv_fp8(self) -> bool:
+        return self.k_cache.dtype == torch.float8_e4m3fn
 
     @property
     def num_seqs(self) -> int:
@@ -85,10 +93,14 @@ def paged_problem(*, seed: int, q_lens, kv_lens, num_q_heads: int, num_kv_heads:
                   head_size: int, block_size: int, dtype: torch.dtype = torch.bfloat16,
                   sigma: float = 1.0, causal: bool = True, scale: float | None = None,
                   permute: bool = True, pool_extra: int = 0, poison: bool = True,
-                  table_pad: int = 0) -> PagedProblem:
+                  table_pad: int = 0, kv_dtype: torch.dtype | None = None) -> PagedProblem:
     """Builds one paged problem on the CPU.  ``q_lens``/``kv_lens`` are lists of
     per-sequence lengths.  ``pool_extra`` unreferenced pages are added to the
-    pool; ``table_pad`` extra -1 columns are added to the block table."""
+    pool; ``table_pad`` extra -1 columns are added to the block table.
+    ``kv_dtype=torch.float8_e4m3fn`` stores the caches as fp8 codes: the same
+    fp32 draws divided by a per-tensor factor sigma * 6 / 448 (so +-6 sigma
+    spans the format), clamped to +-448 and rounded to nearest-even; the
+    factor is returned as ``k_scale`` / ``v_scale``."""
     q_lens = [int(x) for x in q_lens]
     kv_lens = [int(x) for x in kv_lens]
     assert len(q_lens) == len(kv_lens)
@@ -115,17 +127,26 @@ def paged_problem(*, seed: int, q_lens, kv_lens, num_q_heads: int, num_kv_heads:
     total_q = sum(q_lens)
     q = (torch.randn((total_q, H, d), generator=g_val, dtype=torch.float32) * sigma).to(dtype)
 
+    fp8 = kv_dtype == torch.float8_e4m3fn
+    if kv_dtype is not None and not fp8 and kv_dtype != dtype:
+        raise ValueError("kv_dtype is the query dtype or float8_e4m3fn")
+    cdt = torch.float8_e4m3fn if fp8 else dtype
+    kv_scale = sigma * 6.0 / 448.0 if fp8 else 1.0
     fill = _poison_value(dtype) if poison else 0.0
-    k_cache = torch.full((max(n_pages, 1), bs, Hk, d), fill, dtype=dtype)
-    v_cache = torch.full((max(n_pages, 1), bs, Hk, d), fill, dtype=dtype)
+    k_cache = torch.full((max(n_pages, 1), bs, Hk, d), fill, dtype=cdt)
+    v_cache = torch.full((max(n_pages, 1), bs, Hk, d), fill, dtype=cdt)
     for name, cache in (("k", k_cache), ("v", v_cache)):
         for b, sk in enumerate(kv_lens):
             if sk == 0:
                 continue
-            vals = (torch.randn((sk, Hk, d), generator=g_val, dtype=torch.float32) * sigma).to(dtype)
+            vals = torch.randn((sk, Hk, d), generator=g_val, dtype=torch.float32) * sigma
+            if fp8:
+                vals = (vals / kv_scale).clamp(-448.0, 448.0).to(cdt)
+            else:
+                vals = vals.to(dtype)
             npg = pages[b]
             ids = block_table[b, :npg].long()
-            padded = torch.full((npg * bs, Hk, d), fill, dtype=dtype)
+            padded = torch.full((npg * bs, Hk, d), fill, dtype=cdt)
             padded[:sk] = vals
             cache[ids] = padded.view(npg, bs, Hk, d)
 
@@ -139,7 +160,8 @@ def paged_problem(*, seed: int, q_lens, kv_lens, num_q_heads: int, num_kv_heads:
                         query_start_loc=qsl, seq_lens=seq_lens, q_lens=q_lens,
                         kv_lens=kv_lens, num_q_heads=H, num_kv_heads=Hk, head_size=d,
                         block_size=bs, dtype=dtype, scale=float(scale), causal=bool(causal),
-                        meta={"seed": seed, "sigma": sigma, "permute": permute})
+                        meta={"seed": seed, "sigma": sigma, "permute": permute},
+                        k_scale=float(kv_scale), v_scale=float(kv_scale))
 
 
 def random_kv_lens(seed: int, n: int, lo: int, hi: int) -> list:

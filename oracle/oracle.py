@@ -60,11 +60,13 @@ def _load():
         lib.oracle_sdpa_run_ex.restype = ctypes.c_int
         lib.oracle_sdpa_run_ex.argtypes = [P, P, P, P, P, P, i32, P, P, i32, i32, i32,
                                            i32, i32, f64, i32, i32, i32, i32, P, i64, i32,
-                                           i32, i32, f64, P, P]
+                                           i32, i32, f64, P, P, i32, f64, f64]
         lib.oracle_round_f32.restype = None
         lib.oracle_round_f32.argtypes = [P, P, i64, i32, i32]
         lib.oracle_widen16_array.restype = None
         lib.oracle_widen16_array.argtypes = [P, P, i64, i32]
+        lib.oracle_widen8_array.restype = None
+        lib.oracle_widen8_array.argtypes = [P, P, i64]
         _lib = lib
         return lib
 
@@ -77,6 +79,16 @@ def _u16(t) -> np.ndarray:
         import torch
         a = t.detach().contiguous().view(torch.int16).numpy()
     return np.ascontiguousarray(a).view(np.uint16)
+
+
+def _u8(t) -> np.ndarray:
+    """8-bit tensor/array (uint8 or float8) -> contiguous numpy uint8 view of its bits."""
+    if isinstance(t, np.ndarray):
+        a = t
+    else:  # torch tensor (CPU)
+        import torch
+        a = t.detach().contiguous().view(torch.uint8).numpy()
+    return np.ascontiguousarray(a).view(np.uint8)
 
 
 def _i32(t) -> np.ndarray:
@@ -97,7 +109,8 @@ def sdpa(q, k_cache, v_cache, block_table, query_start_loc, seq_lens, *,
          num_q_heads: int, num_kv_heads: int, head_size: int, block_size: int,
          scale: float, causal: bool, dtype: int, rows=None, variant: int = 0,
          param: int = 0, n_threads: int | None = None, want_lse: bool = True,
-         window=(-1, -1), softcap: float = 0.0, alibi_slopes=None, sinks=None):
+         window=(-1, -1), softcap: float = 0.0, alibi_slopes=None, sinks=None,
+         kv_scales=None):
     """fp64 SDPA over the paged problem.
 
     Returns (out, lse): out is float64 [n_rows, head_size] with rows in
@@ -114,9 +127,19 @@ def sdpa(q, k_cache, v_cache, block_table, query_start_loc, seq_lens, *,
     aligned key (-1 = unbounded), ``softcap`` > 0 caps the scaled score at
     c * tanh(s / c), ``alibi_slopes`` [Hq] adds -a_h * |diag - j|, ``sinks``
     [Hq] adds e^(z_h) to the softmax denominator.
+
+    ``kv_scales`` = (k_scale, v_scale) marks the caches as fp8 E4M3 bytes
+    (uint8 or float8_e4m3fn tensors): K = k_scale * e4m3(k), V = v_scale *
+    e4m3(v); ``dtype`` then names the query / output format only.
     """
     lib = _load()
-    qa, ka, va = _u16(q), _u16(k_cache), _u16(v_cache)
+    qa = _u16(q)
+    if kv_scales is None:
+        ka, va = _u16(k_cache), _u16(v_cache)
+        kv_fp8, k_scale, v_scale = 0, 1.0, 1.0
+    else:
+        ka, va = _u8(k_cache), _u8(v_cache)
+        kv_fp8, k_scale, v_scale = 1, float(kv_scales[0]), float(kv_scales[1])
     bt = _i32(block_table)
     if bt.ndim == 1:
         bt = bt.reshape(1, -1)
@@ -150,7 +173,8 @@ def sdpa(q, k_cache, v_cache, block_table, query_start_loc, seq_lens, *,
         float(scale), int(bool(causal)), int(dtype), int(variant), int(param),
         _ptr(rows_a) if rows_a is not None else None, n_rows,
         int(n_threads or default_threads()), int(window[0]), int(window[1]), float(softcap),
-        _ptr(al) if al is not None else None, _ptr(sk) if sk is not None else None)
+        _ptr(al) if al is not None else None, _ptr(sk) if sk is not None else None,
+        kv_fp8, k_scale, v_scale)
     if rc != 0:
         raise ValueError("oracle rejected the problem description")
     return out, lse
@@ -172,4 +196,13 @@ def widen16(bits, dtype: int) -> np.ndarray:
     a = np.ascontiguousarray(np.asarray(bits, dtype=np.uint16))
     out = np.empty(a.shape, dtype=np.float64)
     lib.oracle_widen16_array(_ptr(out), _ptr(a), int(a.size), int(dtype))
+    return out
+
+
+def widen8(bits) -> np.ndarray:
+    """uint8 bit patterns of fp8 E4M3 -> exact float64 values (NaN for S.1111.111)."""
+    lib = _load()
+    a = np.ascontiguousarray(np.asarray(bits, dtype=np.uint8))
+    out = np.empty(a.shape, dtype=np.float64)
+    lib.oracle_widen8_array(_ptr(out), _ptr(a), int(a.size))
     return out

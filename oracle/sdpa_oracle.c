@@ -36,6 +36,9 @@
  *                               away from zero, toward zero.
  *   oracle_widen16           -- exact widening of bf16 / fp16 bit patterns to
  *                               binary64, from the formats' definitions.
+ *   oracle_widen8            -- exact widening of fp8 E4M3 bit patterns (the
+ *                               OCP 8-bit format with 4 exponent bits, bias 7,
+ *                               3 fraction bits, no infinities, S.1111.111 NaN).
  *
  * Feature-flagged variants (variant 0 only).  [ALG] sec. 9 names sinks,
  * ALiBi, softcap, sliding window (and fp8) as flags the dispatcher keeps out
@@ -50,6 +53,10 @@
  *   sink z_h: one more logit in the softmax denominator with no value row,
  *       O = sum_j e^(s_j) V_j / (sum_j e^(s_j) + e^(z_h)); the log-sum-exp
  *       includes it.
+ *   fp8 K/V caches: the caches hold E4M3 bytes and the key and value used
+ *       are the widened byte times a per-tensor factor, K = k_scale * e4m3(k),
+ *       V = v_scale * e4m3(v) (the common "descale" convention); queries and
+ *       outputs keep the 16-bit dtype.
  *
  * Readings where the pages are silent:
  *   - A query row with no visible key (causal with query_len > kv_len, or
@@ -69,6 +76,27 @@ enum { OR_RTNE = 0, OR_RTNA = 1, OR_RTZ = 2 };
 /* ------------------------------------------------------------------------ */
 /* 16-bit formats -> binary64                                               */
 /* ------------------------------------------------------------------------ */
+
+/* E4M3: bit 7 sign, bits 6..3 exponent e (bias 7), bits 2..0 fraction f.
+ * e = 0: subnormal, f/8 * 2^-6.  e >= 1: (1 + f/8) * 2^(e-7), except that
+ * e = 15 with f = 7 is NaN (the format has no infinities; 448 is the largest
+ * finite magnitude). */
+double oracle_widen8(uint8_t b)
+{
+    const int s = (b >> 7) & 1;
+    const int e = (b >> 3) & 15;
+    const int f = b & 7;
+    double mag;
+    if (e == 15 && f == 7) return NAN;
+    if (e == 0) mag = ldexp((double)f / 8.0, -6);
+    else mag = ldexp(1.0 + (double)f / 8.0, e - 7);
+    return s ? -mag : mag;
+}
+
+void oracle_widen8_array(double *out, const uint8_t *in, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i) out[i] = oracle_widen8(in[i]);
+}
 
 /* bf16 is the upper half of a binary32 pattern; fp16 is IEEE binary16
  * (1 sign, 5 exponent bits with bias 15, 10 fraction bits). */
@@ -213,8 +241,8 @@ void oracle_round_f32(uint16_t *out, const float *in, int64_t n, int32_t dtype, 
 
 typedef struct {
     const uint16_t *q;           /* [total_q, Hq, d] */
-    const uint16_t *k_cache;     /* [num_blocks, bs, Hkv, d] */
-    const uint16_t *v_cache;     /* [num_blocks, bs, Hkv, d] */
+    const void *k_cache;         /* [num_blocks, bs, Hkv, d], 16-bit or E4M3 */
+    const void *v_cache;         /* [num_blocks, bs, Hkv, d], 16-bit or E4M3 */
     const int32_t *block_table;  /* [num_seqs, bt_stride] */
     int32_t bt_stride;
     const int32_t *query_start_loc;  /* [num_seqs + 1] */
@@ -228,6 +256,8 @@ typedef struct {
     double softcap;              /* 0 = off */
     const double *alibi;         /* [Hq] slopes or NULL */
     const double *sinks;         /* [Hq] sink logits or NULL */
+    int32_t kv_fp8;              /* 1: caches hold E4M3 bytes */
+    double k_scale, v_scale;     /* factors applied to widened E4M3 K / V */
     const int64_t *rows;         /* optional list of row ids t*Hq + h */
     int64_t n_rows;
     double *out;                 /* [n_rows, d] */
@@ -242,13 +272,14 @@ typedef struct {
 
 /* element (key j of sequence b, kv head kvh, channel c) of a paged cache,
  * found through the block table as in [ALG] sec. 5 */
-static double cache_at(const problem_t *p, const uint16_t *cache, int32_t b,
+static double cache_at(const problem_t *p, const void *cache, double fp8_scale, int32_t b,
                        int64_t j, int32_t kvh, int32_t c)
 {
     int32_t page = p->block_table[(int64_t)b * p->bt_stride + j / p->bs];
     int64_t slot = j % p->bs;
     int64_t idx = (((int64_t)page * p->bs + slot) * p->Hkv + kvh) * p->d + c;
-    return oracle_widen16(cache[idx], p->dtype);
+    if (p->kv_fp8) return fp8_scale * oracle_widen8(((const uint8_t *)cache)[idx]);
+    return oracle_widen16(((const uint16_t *)cache)[idx], p->dtype);
 }
 
 static int32_t seq_of_token(const problem_t *p, int64_t t)
@@ -294,7 +325,7 @@ static void one_row(const problem_t *p, int64_t t, int32_t h, double *o,
     for (int64_t j = lo; j < limit; ++j) {
         double acc = 0.0;
         for (int32_t c = 0; c < d; ++c)
-            acc += qv[c] * cache_at(p, p->k_cache, b, j, kvh, c);
+            acc += qv[c] * cache_at(p, p->k_cache, p->k_scale, b, j, kvh, c);
         double x = p->scale * acc;
         if (p->softcap > 0.0) x = p->softcap * tanh(x / p->softcap);
         if (p->alibi) x -= p->alibi[h] * fabs((double)(diag - j));
@@ -311,7 +342,7 @@ static void one_row(const problem_t *p, int64_t t, int32_t h, double *o,
             double w = exp(s[j] - m);
             den += w;
             for (int32_t c = 0; c < d; ++c)
-                o[c] += w * cache_at(p, p->v_cache, b, j, kvh, c);
+                o[c] += w * cache_at(p, p->v_cache, p->v_scale, b, j, kvh, c);
         }
         for (int32_t c = 0; c < d; ++c) o[c] /= den;
         if (lse) *lse = m + log(den);
@@ -331,7 +362,7 @@ static void one_row(const problem_t *p, int64_t t, int32_t h, double *o,
                 double pj = exp(s[j] - m_new);
                 tsum += pj;
                 for (int32_t c = 0; c < d; ++c)
-                    o[c] += pj * cache_at(p, p->v_cache, b, j, kvh, c);
+                    o[c] += pj * cache_at(p, p->v_cache, p->v_scale, b, j, kvh, c);
             }
             l = alpha * l + tsum;
             m = m_new;
@@ -359,7 +390,7 @@ static void one_row(const problem_t *p, int64_t t, int32_t h, double *o,
                 double w = exp(s[j] - m);
                 den += w;
                 for (int32_t c = 0; c < d; ++c)
-                    po[c] += w * cache_at(p, p->v_cache, b, j, kvh, c);
+                    po[c] += w * cache_at(p, p->v_cache, p->v_scale, b, j, kvh, c);
             }
             for (int32_t c = 0; c < d; ++c) po[c] /= den;
             part_lse[q] = m + log(den);
@@ -438,9 +469,10 @@ static int run_problem(problem_t *p, int32_t n_threads)
 
 /* Common entry.  out is [n_rows, d] (n_rows = total_q * Hq when rows is
  * NULL, in (token, head) order), lse is [n_rows] or NULL.  win_left /
- * win_right = -1, softcap = 0, alibi = sinks = NULL give the plain problem. */
+ * win_right = -1, softcap = 0, alibi = sinks = NULL give the plain problem;
+ * kv_fp8 = 1 reads the caches as E4M3 bytes scaled by k_scale / v_scale. */
 int oracle_sdpa_run_ex(double *out, double *lse,
-                       const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
+                       const uint16_t *q, const void *k_cache, const void *v_cache,
                        const int32_t *block_table, int32_t bt_stride,
                        const int32_t *query_start_loc, const int32_t *seq_lens,
                        int32_t num_seqs, int32_t Hq, int32_t Hkv, int32_t d, int32_t bs,
@@ -448,12 +480,14 @@ int oracle_sdpa_run_ex(double *out, double *lse,
                        int32_t variant, int32_t param,
                        const int64_t *rows, int64_t n_rows, int32_t n_threads,
                        int32_t win_left, int32_t win_right, double softcap,
-                       const double *alibi, const double *sinks)
+                       const double *alibi, const double *sinks,
+                       int32_t kv_fp8, double k_scale, double v_scale)
 {
     problem_t p;
     memset(&p, 0, sizeof(p));
     p.win_left = win_left; p.win_right = win_right; p.softcap = softcap;
     p.alibi = alibi; p.sinks = sinks;
+    p.kv_fp8 = kv_fp8; p.k_scale = k_scale; p.v_scale = v_scale;
     p.q = q; p.k_cache = k_cache; p.v_cache = v_cache;
     p.block_table = block_table; p.bt_stride = bt_stride;
     p.query_start_loc = query_start_loc; p.seq_lens = seq_lens;
@@ -477,5 +511,5 @@ int oracle_sdpa_run(double *out, double *lse,
     return oracle_sdpa_run_ex(out, lse, q, k_cache, v_cache, block_table, bt_stride,
                               query_start_loc, seq_lens, num_seqs, Hq, Hkv, d, bs, scale,
                               causal, dtype, variant, param, rows, n_rows, n_threads,
-                              -1, -1, 0.0, NULL, NULL);
+                              -1, -1, 0.0, NULL, NULL, 0, 1.0, 1.0);
 }
