@@ -18,6 +18,12 @@ attn_fwd_decode_ex, used when any flag is given): ``window=(left, right)``
 sliding window around the aligned key (-1 = unbounded), ``softcap`` > 0,
 ``alibi_slopes`` and ``sinks`` as CUDA fp32 tensors with one entry per query
 head.  Their definitions are in include/attn_fwd.h.
+
+fp8 caches: ``kv_scales=(k_scale, v_scale)`` marks ``k_cache`` / ``v_cache``
+as torch.float8_e4m3fn (or uint8) tensors of E4M3 codes whose values are
+code * k_scale and code * v_scale.  A prefill call then also needs
+``fp8_workspace``, a uint8 CUDA tensor of attn_fp8_prefill_workspace_size()
+bytes (the allocating ``prefill`` creates it).
 """
 from __future__ import annotations
 
@@ -31,7 +37,7 @@ from .build_ext import LIB_PATH
 
 __all__ = ["attn_fwd_prefill", "attn_fwd_dense", "attn_fwd_decode", "attn_fwd_decode_noalloc",
            "has_features", "dense",
-           "attn_decode_workspace_size",
+           "attn_decode_workspace_size", "attn_fp8_prefill_workspace_size",
            "attn_round_f32", "attn_status_string", "attn_abi_version", "prefill", "decode",
            "AttnError", "library_path", "load_library", "RTNE", "RTNA", "RTZ", "OUT_F32"]
 
@@ -82,6 +88,8 @@ def load_library() -> ctypes.CDLL:
                                                   ctypes.c_int, P, ctypes.c_uint64, P]
         lib.attn_decode_workspace_size.restype = sz
         lib.attn_decode_workspace_size.argtypes = [i32, i32, i32, i32]
+        lib.attn_fp8_prefill_workspace_size.restype = sz
+        lib.attn_fp8_prefill_workspace_size.argtypes = [i32, i32, i32, i32, i32]
         lib.attn_fwd_decode.restype = ctypes.c_int
         lib.attn_fwd_decode.argtypes = [P, P, P, P, P, i32, P, i32, i32, i32, i32, i32, i32, i32,
                                         f32, i32, ctypes.c_int, ctypes.c_int, P, P, sz, P, P]
@@ -153,13 +161,15 @@ class _Features(ctypes.Structure):
     """attn_features_t"""
     _fields_ = [("window_left", ctypes.c_int32), ("window_right", ctypes.c_int32),
                 ("softcap", ctypes.c_float), ("alibi_slopes", ctypes.c_void_p),
-                ("sinks", ctypes.c_void_p)]
+                ("sinks", ctypes.c_void_p), ("kv_fp8", ctypes.c_int32),
+                ("k_scale", ctypes.c_float), ("v_scale", ctypes.c_float),
+                ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t)]
 
 
 def _features(num_q_heads: int, window=None, softcap: float = 0.0, alibi_slopes=None,
-              sinks=None):
+              sinks=None, kv_scales=None, fp8_workspace=None):
     """The attn_features_t of a call, or None for a plain call."""
-    if window is None and not softcap and alibi_slopes is None and sinks is None:
+    if not has_features(window, softcap, alibi_slopes, sinks, kv_scales):
         return None
     wl, wr = (-1, -1) if window is None else (int(window[0]), int(window[1]))
     for t, name in ((alibi_slopes, "alibi_slopes"), (sinks, "sinks")):
@@ -167,14 +177,34 @@ def _features(num_q_heads: int, window=None, softcap: float = 0.0, alibi_slopes=
             _dev(t, name, torch.float32)
             if t.numel() != num_q_heads:
                 raise ValueError(f"{name} needs one entry per query head ({num_q_heads})")
+    ws, ws_bytes = None, 0
+    if fp8_workspace is not None:
+        _dev(fp8_workspace, "fp8_workspace")
+        ws, ws_bytes = fp8_workspace.data_ptr(), fp8_workspace.numel() * fp8_workspace.element_size()
+    ks, vs = (1.0, 1.0) if kv_scales is None else (float(kv_scales[0]), float(kv_scales[1]))
     return _Features(wl, wr, float(softcap),
                      None if alibi_slopes is None else alibi_slopes.data_ptr(),
-                     None if sinks is None else sinks.data_ptr())
+                     None if sinks is None else sinks.data_ptr(),
+                     0 if kv_scales is None else 1, ks, vs, ws, ws_bytes)
 
 
-def has_features(window=None, softcap: float = 0.0, alibi_slopes=None, sinks=None) -> bool:
+def has_features(window=None, softcap: float = 0.0, alibi_slopes=None, sinks=None,
+                 kv_scales=None) -> bool:
     """True when a call carries any feature flag."""
-    return not (window is None and not softcap and alibi_slopes is None and sinks is None)
+    return not (window is None and not softcap and alibi_slopes is None and sinks is None and
+                kv_scales is None)
+
+
+_FP8_CACHE_DTYPES = (torch.float8_e4m3fn, torch.uint8)
+
+
+def _cache_dev(t, name, q_dtype, kv_scales):
+    """A K/V cache: the query dtype, or E4M3 codes when kv_scales is given."""
+    if kv_scales is None:
+        return _dev(t, name, q_dtype)
+    _dev(t, name)
+    if t.dtype not in _FP8_CACHE_DTYPES:
+        raise TypeError(f"{name} must be torch.float8_e4m3fn or uint8 with kv_scales, got {t.dtype}")
 
 
 # ----------------------------------------------------------------------------
@@ -195,17 +225,25 @@ def attn_decode_workspace_size(num_seqs: int, num_q_heads: int, head_size: int,
                                                          num_splits))
 
 
+def attn_fp8_prefill_workspace_size(num_seqs: int, max_seqlen_k: int, num_kv_heads: int,
+                                    head_size: int, block_size: int) -> int:
+    return int(load_library().attn_fp8_prefill_workspace_size(num_seqs, max_seqlen_k,
+                                                              num_kv_heads, head_size,
+                                                              block_size))
+
+
 def attn_fwd_prefill(out, q, k_cache, v_cache, block_table, query_start_loc, seq_lens, *,
                      max_seqlen_q: int, max_seqlen_k: int, scale: float, causal: bool,
                      rounding: int = RTNE, lse=None, status=None, stream=None, window=None,
-                     softcap: float = 0.0, alibi_slopes=None, sinks=None) -> None:
+                     softcap: float = 0.0, alibi_slopes=None, sinks=None, kv_scales=None,
+                     fp8_workspace=None) -> None:
     """Calls attn_fwd_prefill (attn_fwd_prefill_ex with feature flags) on torch
     CUDA tensors (shapes as in the C header)."""
     lib = load_library()
     dt = _dtype_code(q.dtype)
     _dev(q, "q")
-    _dev(k_cache, "k_cache", q.dtype)
-    _dev(v_cache, "v_cache", q.dtype)
+    _cache_dev(k_cache, "k_cache", q.dtype, kv_scales)
+    _cache_dev(v_cache, "v_cache", q.dtype, kv_scales)
     _dev(out, "out", torch.float32 if rounding == OUT_F32 else q.dtype)
     _dev(block_table, "block_table", torch.int32)
     _dev(query_start_loc, "query_start_loc", torch.int32)
@@ -226,7 +264,7 @@ def attn_fwd_prefill(out, q, k_cache, v_cache, block_table, query_start_loc, seq
             block_table.shape[1], _ptr(query_start_loc), _ptr(seq_lens), num_seqs,
             int(max_seqlen_q), int(max_seqlen_k), total_q, hq, hkv, d, bs, nb, float(scale),
             int(bool(causal)), dt, int(rounding), _ptr(lse), _ptr(status), _stream_handle(stream))
-    feat = _features(hq, window, softcap, alibi_slopes, sinks)
+    feat = _features(hq, window, softcap, alibi_slopes, sinks, kv_scales, fp8_workspace)
     if feat is None:
         _check(lib.attn_fwd_prefill(*args), "attn_fwd_prefill")
     else:
@@ -280,14 +318,14 @@ def attn_fwd_dense(out, q, k, v, *, scale: float, causal: bool, rounding: int = 
 def attn_fwd_decode(out, q, k_cache, v_cache, block_table, seq_lens, *, max_seqlen_k: int,
                     scale: float, num_splits: int, workspace=None, rounding: int = RTNE,
                     lse=None, status=None, stream=None, window=None, softcap: float = 0.0,
-                    alibi_slopes=None, sinks=None) -> None:
+                    alibi_slopes=None, sinks=None, kv_scales=None) -> None:
     """Calls attn_fwd_decode (attn_fwd_decode_ex with feature flags) on torch
     CUDA tensors (shapes as in the C header)."""
     lib = load_library()
     dt = _dtype_code(q.dtype)
     _dev(q, "q")
-    _dev(k_cache, "k_cache", q.dtype)
-    _dev(v_cache, "v_cache", q.dtype)
+    _cache_dev(k_cache, "k_cache", q.dtype, kv_scales)
+    _cache_dev(v_cache, "v_cache", q.dtype, kv_scales)
     _dev(out, "out", torch.float32 if rounding == OUT_F32 else q.dtype)
     _dev(block_table, "block_table", torch.int32)
     _dev(seq_lens, "seq_lens", torch.int32)
@@ -309,7 +347,7 @@ def attn_fwd_decode(out, q, k_cache, v_cache, block_table, seq_lens, *, max_seql
             block_table.shape[1], _ptr(seq_lens), num_seqs, int(max_seqlen_k), hq, hkv, d, bs, nb,
             float(scale), int(num_splits), dt, int(rounding), _ptr(lse), _ptr(workspace),
             ws_bytes, _ptr(status), _stream_handle(stream))
-    feat = _features(hq, window, softcap, alibi_slopes, sinks)
+    feat = _features(hq, window, softcap, alibi_slopes, sinks, kv_scales)
     if feat is None:
         _check(lib.attn_fwd_decode(*args), "attn_fwd_decode")
     else:
@@ -370,12 +408,19 @@ def prefill(q, k_cache, v_cache, block_table, query_start_loc, seq_lens, *, max_
             rounding: int = RTNE, return_lse: bool = False, status=None, stream=None,
             **features):
     """Returns O (and the log-sum-exp when asked) for a paged prefill problem.
-    ``features``: window, softcap, alibi_slopes, sinks (see the module doc)."""
+    ``features``: window, softcap, alibi_slopes, sinks, kv_scales (see the
+    module doc); with kv_scales the fp8 workspace is allocated here."""
     if scale is None:
         scale = q.shape[-1] ** -0.5
     out = torch.empty(q.shape, dtype=torch.float32 if rounding == OUT_F32 else q.dtype,
                       device=q.device)
     lse = torch.empty(q.shape[:2], dtype=torch.float32, device=q.device) if return_lse else None
+    if features.get("kv_scales") is not None and features.get("fp8_workspace") is None:
+        nbytes = attn_fp8_prefill_workspace_size(seq_lens.shape[0], int(max_seqlen_k),
+                                                 k_cache.shape[2], k_cache.shape[3],
+                                                 k_cache.shape[1])
+        features = dict(features, fp8_workspace=torch.empty(max(nbytes, 1), dtype=torch.uint8,
+                                                            device=q.device))
     attn_fwd_prefill(out, q, k_cache, v_cache, block_table, query_start_loc, seq_lens,
                      max_seqlen_q=max_seqlen_q, max_seqlen_k=max_seqlen_k, scale=scale,
                      causal=causal, rounding=rounding, lse=lse, status=status, stream=stream,

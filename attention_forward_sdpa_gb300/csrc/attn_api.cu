@@ -64,6 +64,10 @@ struct Features {
   float softcap = 0.f;
   const float* alibi = nullptr;
   const float* sinks = nullptr;
+  bool kv_fp8 = false;
+  float k_scale = 1.f, v_scale = 1.f;
+  void* workspace = nullptr;
+  size_t workspace_bytes = 0;
   bool any() const { return win_left >= 0 || win_right >= 0 || softcap > 0.f || alibi || sinks; }
 };
 
@@ -80,7 +84,40 @@ attn_status_t read_features(const attn_features_t* f, Features& out) {
   out.softcap = f->softcap;
   out.alibi = f->alibi_slopes;
   out.sinks = f->sinks;
+  if (f->kv_fp8 != 0 && f->kv_fp8 != 1) return ATTN_ERR_INVALID_ARG;
+  if (f->kv_fp8) {
+    if (!valid_scale(f->k_scale) || !valid_scale(f->v_scale)) return ATTN_ERR_INVALID_ARG;
+    out.kv_fp8 = true;
+    out.k_scale = f->k_scale;
+    out.v_scale = f->v_scale;
+    out.workspace = f->workspace;
+    out.workspace_bytes = f->workspace_bytes;
+  }
   return ATTN_OK;
+}
+
+// Layout of the fp8 prefill workspace: widened K pages, widened V pages,
+// block table, each at a 256-byte boundary.
+struct Fp8Workspace {
+  size_t k_off, v_off, table_off, total;
+  int64_t pages_per_seq, n_pages, page_elems;
+};
+
+bool fp8_workspace_layout(int32_t num_seqs, int32_t max_seqlen_k, int32_t num_kv_heads,
+                          int32_t head_size, int32_t block_size, Fp8Workspace& w) {
+  if (num_seqs <= 0 || max_seqlen_k < 0 || num_kv_heads <= 0 || head_size <= 0 || block_size <= 0)
+    return false;
+  auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+  w.pages_per_seq = ((int64_t)max_seqlen_k + block_size - 1) / block_size;
+  if (w.pages_per_seq < 1) w.pages_per_seq = 1;
+  w.n_pages = (int64_t)num_seqs * w.pages_per_seq;
+  w.page_elems = (int64_t)block_size * num_kv_heads * head_size;
+  const size_t cache_bytes = up((size_t)w.n_pages * (size_t)w.page_elems * 2);
+  w.k_off = 0;
+  w.v_off = cache_bytes;
+  w.table_off = 2 * cache_bytes;
+  w.total = w.table_off + up((size_t)w.n_pages * 4);
+  return true;
 }
 
 void set_features(attn::PrefillParams& p, const Features& f, float scale) {
@@ -91,6 +128,7 @@ void set_features(attn::PrefillParams& p, const Features& f, float scale) {
   p.sinks = f.sinks;
   p.scale = scale;
   p.score_xform = (f.softcap > 0.f || f.alibi) ? 1 : 0;
+  p.out_scale = f.kv_fp8 ? f.v_scale : 1.f;
 }
 
 // Prefill grid (x: head units, z: row units; y is the sequence).  Head sizes
@@ -122,6 +160,17 @@ bool encode_tiled(CUtensorMap* map, bool bf16, int rank, const cuuint64_t* dims,
             (cuuint32_t)rank, const_cast<void*>(base), dims, strides_bytes, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool encode_tiled_u8(CUtensorMap* map, int rank, const cuuint64_t* dims,
+                     const cuuint64_t* strides_bytes, const cuuint32_t* box, const void* base,
+                     CUtensorMapSwizzle swz) {
+  EncodeTiledFn fn = get_encode_fn();
+  if (!fn) return false;
+  cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, (cuuint32_t)rank, const_cast<void*>(base), dims,
+            strides_bytes, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 int device_sm_count() {
@@ -175,6 +224,18 @@ int decode_prepare_and_launch(DecodeParams& p, int head_size, bool bf16, void* w
   const cuuint64_t d = (cuuint64_t)head_size;
   const cuuint64_t slot_stride = d * 2 * (cuuint64_t)p.num_kv_heads;
   const cuuint64_t block_stride = slot_stride * (cuuint64_t)p.block_size;
+  if (p.kv_fp8) {
+    // fp8 codes as (channel, slot, head, page): a box of all 128 codes x 16
+    // slots x F heads lands as 16F rows of 128 bytes (K and V alike)
+    const cuuint64_t dims[4] = {d, (cuuint64_t)p.block_size, (cuuint64_t)p.num_kv_heads,
+                                (cuuint64_t)p.num_blocks};
+    const cuuint64_t strides[3] = {d * (cuuint64_t)p.num_kv_heads, d,
+                                   d * (cuuint64_t)p.num_kv_heads * (cuuint64_t)p.block_size};
+    const cuuint32_t box[4] = {128, 16, (cuuint32_t)p.kv_per_item, 1};
+    if (!encode_tiled_u8(&p.tm_k, 4, dims, strides, box, p.k_cache, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_tiled_u8(&p.tm_v, 4, dims, strides, box, p.v_cache, CU_TENSOR_MAP_SWIZZLE_128B))
+      return ATTN_ERR_CUDA;
+  }
   {
     const cuuint64_t dims[3] = {d, (cuuint64_t)p.num_q_heads, (cuuint64_t)p.num_seqs};
     const cuuint64_t strides[2] = {d * 2, d * 2 * (cuuint64_t)p.num_q_heads};
@@ -182,7 +243,7 @@ int decode_prepare_and_launch(DecodeParams& p, int head_size, bool bf16, void* w
     if (!encode_tiled(&p.tm_q, bf16, 3, dims, strides, box, p.q, CU_TENSOR_MAP_SWIZZLE_128B))
       return ATTN_ERR_CUDA;
   }
-  {
+  if (!p.kv_fp8) {
     // K as (channel, slot, head, page): a box of 16 slots x F heads lands as
     // 16F consecutive rows of 64 channels
     const cuuint64_t dims[4] = {d, (cuuint64_t)p.block_size, (cuuint64_t)p.num_kv_heads,
@@ -192,7 +253,7 @@ int decode_prepare_and_launch(DecodeParams& p, int head_size, bool bf16, void* w
     if (!encode_tiled(&p.tm_k, bf16, 4, dims, strides, box, p.k_cache, CU_TENSOR_MAP_SWIZZLE_128B))
       return ATTN_ERR_CUDA;
   }
-  {
+  if (!p.kv_fp8) {
     // V as (channel in half, slot, channel half, head, page): one box brings
     // both channel halves of 16 slots x F heads
     const cuuint64_t dims[5] = {64, (cuuint64_t)p.block_size, 2, (cuuint64_t)p.num_kv_heads,
@@ -215,7 +276,7 @@ int decode_prepare_and_launch(DecodeParams& p, int head_size, bool bf16, void* w
 
 extern "C" {
 
-int32_t attn_abi_version(void) { return 1; }
+int32_t attn_abi_version(void) { return 2; }
 
 const char* attn_status_string(attn_status_t s) {
   switch (s) {
@@ -269,8 +330,41 @@ attn_status_t prefill_impl(void* out, const void* q, const void* k_cache, const 
   prefill_grid(head_size, pair_heads, num_q_heads, row_blocks, gx, gz);
   if (num_seqs > 65535 || gz > 65535 || gx > 2147483647) return ATTN_ERR_UNSUPPORTED;
 
+  // fp8 caches: the K factor joins tau, the V factor scales the output
+  const float scale_eff = feat.kv_fp8 ? scale * feat.k_scale : scale;
+  if (!valid_scale(scale_eff)) return ATTN_ERR_INVALID_ARG;
+  Fp8Workspace fw;
+  if (feat.kv_fp8) {
+    if (!fp8_workspace_layout(num_seqs, max_seqlen_k, num_kv_heads, head_size, block_size, fw))
+      return ATTN_ERR_INVALID_ARG;
+    if (fw.n_pages > 2147483647) return ATTN_ERR_UNSUPPORTED;
+    if (!feat.workspace || feat.workspace_bytes < fw.total ||
+        (reinterpret_cast<uintptr_t>(feat.workspace) & 255u))
+      return ATTN_ERR_WORKSPACE;
+  }
+
   attn_status_t st = check_device();
   if (st != ATTN_OK) return st;
+
+  if (feat.kv_fp8) {
+    // widen the referenced pages into the workspace, then run the 16-bit
+    // path on that copy through its identity block table
+    uint8_t* ws = static_cast<uint8_t*>(feat.workspace);
+    void* k16 = ws + fw.k_off;
+    void* v16 = ws + fw.v_off;
+    int32_t* table = reinterpret_cast<int32_t*>(ws + fw.table_off);
+    cudaError_t e = attn::launch_kv_widen(k_cache, v_cache, block_table, block_table_stride,
+                                          seq_lens, num_seqs, (int32_t)fw.pages_per_seq,
+                                          block_size, num_blocks, fw.page_elems,
+                                          dtype == ATTN_BF16, k16, v16, table, status_dev,
+                                          static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return ATTN_ERR_CUDA;
+    k_cache = k16;
+    v_cache = v16;
+    block_table = table;
+    block_table_stride = (int32_t)fw.pages_per_seq;
+    num_blocks = (int32_t)fw.n_pages;
+  }
 
   attn::PrefillParams p;
   std::memset(&p, 0, sizeof(p));
@@ -317,10 +411,10 @@ attn_status_t prefill_impl(void* out, const void* q, const void* k_cache, const 
   p.pair_heads = pair_heads ? 1 : 0;
   p.causal = causal;
   p.rounding = (int32_t)rounding;
-  p.scale_log2 = scale * kLog2e;
+  p.scale_log2 = scale_eff * kLog2e;
   p.wait_limit_ns = wait_limit_ns;
   p.stall_producer = stall_producer;
-  set_features(p, feat, scale);
+  set_features(p, feat, scale_eff);
 
   dim3 grid((unsigned)gx, (unsigned)num_seqs, (unsigned)gz);
   cudaError_t e = attn::launch_prefill(p, head_size, bf16, grid, static_cast<cudaStream_t>(stream));
@@ -388,6 +482,7 @@ attn_status_t attn_fwd_dense_ex(void* out, const void* q, const void* k, const v
   // ---- host-side validation (no CUDA call before this block ends)
   Features feat;
   if (read_features(features, feat) != ATTN_OK) return ATTN_ERR_INVALID_ARG;
+  if (feat.kv_fp8) return ATTN_ERR_UNSUPPORTED;   // fp8 caches: paged prefill and decode only
   if (batch < 0 || seqlen_q < 0 || seqlen_k < 0) return ATTN_ERR_INVALID_ARG;
   if (num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0) return ATTN_ERR_INVALID_ARG;
   if (dtype != ATTN_F16 && dtype != ATTN_BF16) return ATTN_ERR_INVALID_ARG;
@@ -496,6 +591,14 @@ size_t attn_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t
   return rows * (size_t)head_size * sizeof(float) + rows * 2 * sizeof(float) + counter_bytes;
 }
 
+size_t attn_fp8_prefill_workspace_size(int32_t num_seqs, int32_t max_seqlen_k,
+                                       int32_t num_kv_heads, int32_t head_size,
+                                       int32_t block_size) {
+  Fp8Workspace w;
+  if (!fp8_workspace_layout(num_seqs, max_seqlen_k, num_kv_heads, head_size, block_size, w)) return 0;
+  return w.total;
+}
+
 attn_status_t attn_fwd_decode_ex(void* out, const void* q, const void* k_cache,
                                  const void* v_cache, const int32_t* block_table,
                                  int32_t block_table_stride, const int32_t* seq_lens,
@@ -548,8 +651,13 @@ attn_status_t attn_fwd_decode_ex(void* out, const void* q, const void* k_cache,
   p.num_blocks = num_blocks;
   p.num_splits = num_splits;
   p.rounding = (int32_t)rounding;
-  p.scale_log2 = scale * kLog2e;
-  p.scale = scale;
+  // fp8 caches: the K factor joins tau, the V factor scales the output
+  const float scale_eff = feat.kv_fp8 ? scale * feat.k_scale : scale;
+  if (!valid_scale(scale_eff)) return ATTN_ERR_INVALID_ARG;
+  p.scale_log2 = scale_eff * kLog2e;
+  p.scale = scale_eff;
+  p.kv_fp8 = feat.kv_fp8 ? 1 : 0;
+  p.out_scale = feat.kv_fp8 ? feat.v_scale : 1.f;
   p.win_left = feat.win_left;      // the right bound never cuts a decode row (diag = kv_len - 1)
   p.softcap = feat.softcap;
   p.alibi = feat.alibi;

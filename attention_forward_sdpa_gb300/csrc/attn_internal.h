@@ -54,6 +54,7 @@ struct PrefillParams {
   float scale;          // tau, for the score rewrite
   const float* alibi;
   const float* sinks;
+  float out_scale;      // factor on the normalised output (fp8 V factor; 1 otherwise)
 };
 
 struct DecodeParams {
@@ -93,6 +94,10 @@ struct DecodeParams {
   float scale;
   const float* alibi;
   const float* sinks;
+  // fp8 caches: K/V hold E4M3 codes; the K factor is folded into scale and
+  // scale_log2, the V factor is out_scale (applied to the normalised output)
+  int32_t kv_fp8;
+  float out_scale;
 };
 
 // Launchers return a cudaError_t from the launch.
@@ -115,6 +120,10 @@ int decode_prepare_and_launch(DecodeParams& p, int head_size, bool bf16, void* w
 bool encode_tiled(CUtensorMap* map, bool bf16, int rank, const cuuint64_t* dims,
                   const cuuint64_t* strides_bytes, const cuuint32_t* box, const void* base,
                   CUtensorMapSwizzle swz);
+// The same for a tensor of bytes (fp8 codes).
+bool encode_tiled_u8(CUtensorMap* map, int rank, const cuuint64_t* dims,
+                     const cuuint64_t* strides_bytes, const cuuint32_t* box, const void* base,
+                     CUtensorMapSwizzle swz);
 int device_sm_count();
 
 // Opts `kernel` in to `bytes` of dynamic shared memory on the current device.
@@ -135,6 +144,17 @@ cudaError_t ensure_dynamic_smem(Kernel kernel, int bytes, std::atomic<uint64_t>&
 
 cudaError_t launch_round(void* out, const float* in, int64_t n, bool bf16, int mode,
                          cudaStream_t stream);
+
+// fp8 prefill: widens the pages that each sequence references (E4M3 codes ->
+// exact 16-bit values) into a dense page array, page (b, p) at index
+// b * pages_per_seq + p, and writes the matching identity block table
+// [num_seqs, pages_per_seq].  A referenced page id outside [0, num_blocks)
+// is reported on the status word and its copy is zero.
+cudaError_t launch_kv_widen(const void* k8, const void* v8, const int32_t* block_table,
+                            int32_t bt_stride, const int32_t* seq_lens, int32_t num_seqs,
+                            int32_t pages_per_seq, int32_t block_size, int32_t num_blocks,
+                            int64_t page_elems, bool bf16, void* k16, void* v16,
+                            int32_t* table_out, int32_t* status, cudaStream_t stream);
 
 // In-kernel error codes written to the status word (same values as the
 // public attn_status_t).

@@ -123,6 +123,7 @@ extern "C" attn_status_t attn_fwd_decode_noalloc(
   p.scale_log2 = scale * 1.4426950408889634f;
   p.scale = scale;
   p.win_left = -1;   // no feature flags on this entry point
+  p.out_scale = 1.f;
   return (attn_status_t)attn::decode_prepare_and_launch(p, head_size, dtype == ATTN_BF16, scratch,
                                                         static_cast<cudaStream_t>(stream));
 }

@@ -24,6 +24,7 @@
 // fixed order) and the elementwise rounding kernel behind attn_round_f32.
 
 #include <algorithm>
+#include <type_traits>
 
 #include "attn_internal.h"
 #include "round16.cuh"
@@ -112,6 +113,36 @@ __device__ __forceinline__ void load_row(const uint16_t* __restrict__ src, float
   }
 }
 
+// Two E4M3 codes (low byte first) -> two floats.  The conversion to f16x2 is
+// exact (every E4M3 value is an fp16 normal or zero), and so is the widening.
+__device__ __forceinline__ void widen_e4m3x2(uint32_t two_codes, float& lo, float& hi) {
+  uint32_t h;
+  const uint16_t c = (uint16_t)two_codes;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"(c));
+  const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&h));
+  lo = a.x;
+  hi = a.y;
+}
+
+// DPL fp8 codes of a lane's channels -> floats (fp8 caches)
+template <int DPL>
+__device__ __forceinline__ void load_row8(const uint8_t* __restrict__ src, float (&x)[DPL]) {
+  if constexpr (DPL == 8) {
+    const uint2 w = __ldg(reinterpret_cast<const uint2*>(src));
+    widen_e4m3x2(w.x, x[0], x[1]);
+    widen_e4m3x2(w.x >> 16, x[2], x[3]);
+    widen_e4m3x2(w.y, x[4], x[5]);
+    widen_e4m3x2(w.y >> 16, x[6], x[7]);
+  } else if constexpr (DPL == 4) {
+    const uint32_t w = __ldg(reinterpret_cast<const uint32_t*>(src));
+    widen_e4m3x2(w, x[0], x[1]);
+    widen_e4m3x2(w >> 16, x[2], x[3]);
+  } else {
+    const uint32_t w = __ldg(reinterpret_cast<const uint16_t*>(src));
+    widen_e4m3x2(w, x[0], x[1]);
+  }
+}
+
 // Keys of split s of a sequence of length Sk: [s*per, min(Sk, (s+1)*per)) with
 // per = ceil(ceil(Sk / splits) / 16) * 16.
 __device__ __forceinline__ void split_range(int Sk, int splits, int s, int& k0, int& k1) {
@@ -132,8 +163,9 @@ __device__ __forceinline__ void store_out(void* out, int64_t idx, const float* v
   }
 }
 
-template <int D, bool BF16, int GH>
+template <int D, bool BF16, int GH, bool KV8>
 __global__ void __launch_bounds__(kDecWarps * 32) decode_split_kernel(const __grid_constant__ DecodeParams p) {
+  using KvT = std::conditional_t<KV8, uint8_t, uint16_t>;   // cache element (fp8 code or 16-bit)
   constexpr int DPL = D / 32;             // channels per lane
   constexpr int CK = (GH <= 4 && D <= 128) ? 16 : 8;    // keys per chunk
   constexpr int N = CK * GH;              // dot products per chunk
@@ -189,8 +221,8 @@ __global__ void __launch_bounds__(kDecWarps * 32) decode_split_kernel(const __gr
   const int bs = p.block_size;
   const int32_t* bt = p.block_table + (int64_t)b * p.bt_stride;
   const int64_t slot_stride = (int64_t)p.num_kv_heads * D;  // elements between consecutive slots
-  const uint16_t* kc = static_cast<const uint16_t*>(p.k_cache);
-  const uint16_t* vc = static_cast<const uint16_t*>(p.v_cache);
+  const KvT* kc = static_cast<const KvT*>(p.k_cache);
+  const KvT* vc = static_cast<const KvT*>(p.v_cache);
   const float sl2 = p.scale_log2;
 
   for (int k0 = k_begin + warp * CK; k0 < k_end; k0 += kDecWarps * CK) {
@@ -206,7 +238,10 @@ __global__ void __launch_bounds__(kDecWarps * 32) decode_split_kernel(const __gr
     float kx[CK][DPL];
 #pragma unroll
     for (int r = 0; r < CK; ++r) {
-      if (r < nv) load_row<BF16, DPL>(kc + base + r * slot_stride, kx[r]);
+      if (r < nv) {
+        if constexpr (KV8) load_row8<DPL>(kc + base + r * slot_stride, kx[r]);
+        else load_row<BF16, DPL>(kc + base + r * slot_stride, kx[r]);
+      }
       else
 #pragma unroll
         for (int e = 0; e < DPL; ++e) kx[r][e] = 0.f;
@@ -271,7 +306,10 @@ __global__ void __launch_bounds__(kDecWarps * 32) decode_split_kernel(const __gr
     float vx[CK][DPL];
 #pragma unroll
     for (int r = 0; r < CK; ++r) {
-      if (r < nv) load_row<BF16, DPL>(vc + base + r * slot_stride, vx[r]);
+      if (r < nv) {
+        if constexpr (KV8) load_row8<DPL>(vc + base + r * slot_stride, vx[r]);
+        else load_row<BF16, DPL>(vc + base + r * slot_stride, vx[r]);
+      }
       else
 #pragma unroll
         for (int e = 0; e < DPL; ++e) vx[r][e] = 0.f;
@@ -323,6 +361,7 @@ __global__ void __launch_bounds__(kDecWarps * 32) decode_split_kernel(const __gr
         v = L > 0.f ? acc / L : 0.f;
         lse_v = L > 0.f ? M * kLn2 + logf(L) : -INFINITY;
       }
+      v *= p.out_scale;   // fp8 V factor (1 otherwise)
       store_out<BF16>(p.out, row * D + e, &v, 1, p.rounding);
       if (e == 0 && p.lse) p.lse[row] = lse_v;
     } else {
@@ -410,6 +449,7 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(const __grid_consta
   float inv, lse_v;
   finish_row(M == -INFINITY ? -INFINITY : Mu, L, p.sinks ? p.sinks[row % p.num_q_heads] : -INFINITY,
              inv, lse_v);
+  inv *= p.out_scale;   // fp8 V factor (1 otherwise)
 #pragma unroll
   for (int e = 0; e < DPL; ++e) acc[e] *= inv;
   store_out<BF16>(p.out, row * D + lane * DPL, acc, DPL, p.rounding);
@@ -427,7 +467,8 @@ template <int D, bool BF16, int GH>
 cudaError_t launch_decode_t(const DecodeParams& p, cudaStream_t stream) {
   const int G = p.num_q_heads / p.num_kv_heads;
   dim3 grid(p.num_splits, p.num_kv_heads * (G / GH), p.num_seqs);
-  decode_split_kernel<D, BF16, GH><<<grid, kDecWarps * 32, 0, stream>>>(p);
+  if (p.kv_fp8) decode_split_kernel<D, BF16, GH, true><<<grid, kDecWarps * 32, 0, stream>>>(p);
+  else decode_split_kernel<D, BF16, GH, false><<<grid, kDecWarps * 32, 0, stream>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || p.num_splits == 1) return e;
   return launch_combine_t<D, BF16>(p, stream);

@@ -29,6 +29,10 @@
 //     exp2, the running denominators, write P^T, rescale O^T when needed, and
 //     at the end of an item write the partial state (un-normalised o, max in
 //     log2 units, denominator) -- or, with one split, the rounded output.
+//   * fp8 caches (E4M3 codes): TMA lands 128-byte rows of codes in staging
+//     tiles, warps 6-9 widen each row exactly into the 16-bit ring tile the
+//     MMAs read (one E4M3 byte per element is read from HBM instead of two);
+//     the K factor is folded into tau, the V factor into the output.
 // Every wait is bounded (see sm103_ptx.cuh); the CTA-wide exchange of the
 // softmax warps also goes through an mbarrier so that it is bounded.
 
@@ -42,8 +46,6 @@ namespace {
 
 constexpr int kD = 128;                 // head size handled here
 constexpr int kRows = 128;              // tile rows: 16-key boxes x F heads x 16 keys
-constexpr int kThreads = 192;
-constexpr int kSlots = 6;               // K/V ring slots of one tile each
 constexpr int kItemRing = 4;
 constexpr int kTileBytes = kRows * kD * 2;      // 32 KB
 constexpr int kHalfBytes = kRows * 128;         // K: 128 rows x 64 channels
@@ -65,25 +67,67 @@ struct ItemEntry {
   int sk;      // the sequence's KV length (its decode row is aligned with key sk - 1)
 };
 
-constexpr int kRingOff = 0;
-constexpr int kQOff = kRingOff + kSlots * kTileBytes;
-constexpr int kPOff = kQOff + 2 * kQBytes;
-constexpr int kRedOff = kPOff + 2 * kPBytes;            // float [2][8 groups][16]
-constexpr int kLRedOff = kRedOff + 2 * 8 * 16 * 4;      // float [2][8 groups][16]
-constexpr int kItemOff = kLRedOff + 2 * 8 * 16 * 4;     // ItemEntry [kItemRing]
-constexpr int kSeqOff = kItemOff + kItemRing * (int)sizeof(ItemEntry);
-constexpr int kOrderOff = kSeqOff + kSeqCache * 4;
-constexpr int kFlagOff = kOrderOff + kSortMax * 4;          // int [3]
-constexpr int kBarOff = kFlagOff + 16;
-// barriers: kv_full[kSlots] kv_empty[kSlots] q_full[2] q_empty[2] s_full[2]
-//           p_full[2] pv_done item_full[R] item_empty[R] mma_done red
-constexpr int kNumBars = 2 * kSlots + 2 + 2 + 2 + 2 + 1 + 2 * kItemRing + 1 + 1;
-constexpr int kMiscOff = kBarOff + kNumBars * 8;
-constexpr int kSmemBytes = kMiscOff + 16 + 1024;
+constexpr int kStage8Bytes = kRows * kD;       // an fp8 tile: 128 rows x 128 codes (16 KB)
+
+// Shared-memory layout.  With 16-bit caches the ring holds six tiles.  With
+// fp8 caches (KV8) TMA lands the codes in four 16 KB staging tiles, four
+// converter warps widen them into a ring of four 16-bit tiles (the layout
+// the MMAs read), and the CTA has 320 threads instead of 192.
+template <bool KV8>
+struct Lay {
+  static constexpr int kThreads = KV8 ? 320 : 192;
+  static constexpr int kSlots = KV8 ? 4 : 6;     // 16-bit K/V ring slots of one tile each
+  static constexpr int kStages = KV8 ? 4 : 0;    // fp8 staging slots
+  static constexpr int kRingOff = 0;
+  static constexpr int kStageOff = kRingOff + kSlots * kTileBytes;
+  static constexpr int kQOff = kStageOff + kStages * kStage8Bytes;
+  static constexpr int kPOff = kQOff + 2 * kQBytes;
+  static constexpr int kRedOff = kPOff + 2 * kPBytes;          // float [2][8 groups][16]
+  static constexpr int kLRedOff = kRedOff + 2 * 8 * 16 * 4;    // float [2][8 groups][16]
+  static constexpr int kItemOff = kLRedOff + 2 * 8 * 16 * 4;   // ItemEntry [kItemRing]
+  static constexpr int kSeqOff = kItemOff + kItemRing * (int)sizeof(ItemEntry);
+  static constexpr int kOrderOff = kSeqOff + kSeqCache * 4;
+  static constexpr int kFlagOff = kOrderOff + kSortMax * 4;    // int [3]
+  static constexpr int kBarOff = kFlagOff + 16;
+  // barriers: kv_full[kSlots] kv_empty[kSlots] q_full[2] q_empty[2] s_full[2]
+  //           p_full[2] pv_done item_full[R] item_empty[R] mma_done red
+  //           stage_full[kStages] stage_empty[kStages]
+  static constexpr int kNumBars = 2 * kSlots + 2 + 2 + 2 + 2 + 1 + 2 * kItemRing + 1 + 1 +
+                                  2 * kStages;
+  static constexpr int kMiscOff = kBarOff + kNumBars * 8;
+  static constexpr int kSmemBytes = kMiscOff + 16 + 1024;
+};
 constexpr uint32_t kTmemCols = 64;      // S^T x 2 (16 columns each), O^T (16)
 constexpr uint32_t kOCol = 32u;
 
 __device__ __forceinline__ uint32_t s_col(uint32_t g) { return (g & 1u) ? 16u : 0u; }
+
+// Two E4M3 codes (low byte -> low half) to two 16-bit values of the query
+// format.  E4M3 -> f16x2 is exact in hardware; f16 -> f32 -> bf16 is exact
+// for these values (at most 4 significant bits).
+template <bool BF16>
+__device__ __forceinline__ uint32_t widen_e4m3x2(uint32_t two_codes) {
+  uint32_t h;
+  const uint16_t c = (uint16_t)two_codes;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"(c));
+  if constexpr (!BF16) return h;
+  const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h));
+  const __nv_bfloat162 b = __floats2bfloat162_rn(f.x, f.y);
+  return *reinterpret_cast<const uint32_t*>(&b);
+}
+
+// 16 codes -> 16 values in element order (lo: codes 0-7, hi: codes 8-15)
+template <bool BF16>
+__device__ __forceinline__ void widen_e4m3x16(const uint4 w, uint4& lo, uint4& hi) {
+  lo.x = widen_e4m3x2<BF16>(w.x);
+  lo.y = widen_e4m3x2<BF16>(w.x >> 16);
+  lo.z = widen_e4m3x2<BF16>(w.y);
+  lo.w = widen_e4m3x2<BF16>(w.y >> 16);
+  hi.x = widen_e4m3x2<BF16>(w.z);
+  hi.y = widen_e4m3x2<BF16>(w.z >> 16);
+  hi.z = widen_e4m3x2<BF16>(w.w);
+  hi.w = widen_e4m3x2<BF16>(w.w >> 16);
+}
 
 __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
   const uint64_t t0 = global_timer_ns();
@@ -109,13 +153,20 @@ __device__ __forceinline__ uint32_t p_offset(int q, int r) {
   return (uint32_t)(half * 2048 + q * 128 + chunk * 16 + (c & 7) * 2);
 }
 
-template <bool BF16, int GH>
-__global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_constant__ DecodeParams p) {
+template <bool BF16, int GH, bool KV8>
+__global__ void __launch_bounds__(Lay<KV8>::kThreads, 1) decode_tc_kernel(const __grid_constant__ DecodeParams p) {
+  using L = Lay<KV8>;
+  constexpr int kThreads = L::kThreads, kSlots = L::kSlots, kStages = L::kStages;
+  constexpr int kRingOff = L::kRingOff, kStageOff = L::kStageOff, kQOff = L::kQOff;
+  constexpr int kPOff = L::kPOff, kRedOff = L::kRedOff, kLRedOff = L::kLRedOff;
+  constexpr int kItemOff = L::kItemOff, kSeqOff = L::kSeqOff, kOrderOff = L::kOrderOff;
+  constexpr int kFlagOff = L::kFlagOff, kBarOff = L::kBarOff, kMiscOff = L::kMiscOff;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* smem = smem_raw + (base - raw);
   const uint32_t sRing = base + kRingOff;
+  const uint32_t sStage = base + kStageOff;
   const uint32_t sQ = base + kQOff;
   const uint32_t sP = base + kPOff;
   float* red = reinterpret_cast<float*>(smem + kRedOff);
@@ -135,6 +186,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
   const uint32_t bar_item_empty = bar_item_full + 8u * kItemRing;
   const uint32_t bar_mma_done = bar_item_empty + 8u * kItemRing;
   const uint32_t bar_red = bar_mma_done + 8u;
+  const uint32_t bar_st_full = bar_red + 8u;                 // fp8: staging tile landed
+  const uint32_t bar_st_empty = bar_st_full + 8u * kStages;  // fp8: staging tile widened
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kMiscOff);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kMiscOff + 4);
 
@@ -149,8 +202,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kSlots; ++s) {
-      mbar_init(bar_kv_full + 8u * s, 1);
+      // fp8: a ring tile is complete when the 128 converter threads arrive
+      mbar_init(bar_kv_full + 8u * s, KV8 ? 128 : 1);
       mbar_init(bar_kv_empty + 8u * s, 1);
+    }
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(bar_st_full + 8u * s, 1);
+      mbar_init(bar_st_empty + 8u * s, 128);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar_q_full + 8u * i, 1);
@@ -161,7 +219,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
     mbar_init(bar_pv_done, 1);
     for (int i = 0; i < kItemRing; ++i) {
       mbar_init(bar_item_full + 8u * i, 1);
-      mbar_init(bar_item_empty + 8u * i, 1 + 4);
+      mbar_init(bar_item_empty + 8u * i, 1 + 4 + (KV8 ? 4 : 0));
     }
     mbar_init(bar_mma_done, 1);
     mbar_init(bar_red, 128);
@@ -300,6 +358,25 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
           const int page = set ? pg[1] : pg[0];
           const int row = set ? rw[1] : rw[0];
           for (int kind = 0; kind < 2; ++kind) {
+            if constexpr (KV8) {
+              // fp8: one box of 128 codes x 16 slots x F heads per 16 keys
+              // lands as 16F rows of 128 bytes in a staging tile
+              const uint32_t s8 = fills % kStages;
+              if (fills >= kStages &&
+                  !mbar_wait(bar_st_empty + 8u * s8, ((fills / kStages) - 1) & 1, abort_flag)) {
+                ok = false;
+                break;
+              }
+              const uint32_t bar = bar_st_full + 8u * s8;
+              if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)(nbox * F * 2048));
+              __syncwarp();
+              if (mine)
+                tma_load_4d(sStage + s8 * kStage8Bytes + j * F * 2048, kind == 0 ? &p.tm_k : &p.tm_v,
+                            bar, 0, row, kvh0, page);
+              last_fill[s8] = fills + 1;
+              ++fills;
+              continue;
+            }
             const uint32_t s = fills % kSlots;
             if (fills >= kSlots &&
                 !mbar_wait(bar_kv_empty + 8u * s, ((fills / kSlots) - 1) & 1, abort_flag)) {
@@ -330,8 +407,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
     }
     // no copy may still be in flight into this CTA's shared memory
     if (lane == 0) {
-      for (int s = 0; s < kSlots; ++s)
-        if (last_fill[s] > 0) drain_wait(bar_kv_full + 8u * s, (last_fill[s] - 1) / kSlots & 1);
+      // (fp8: the copies go to the staging tiles)
+      constexpr int kN = KV8 ? kStages : kSlots;
+      const uint32_t full = KV8 ? bar_st_full : bar_kv_full;
+      for (int s = 0; s < kN; ++s)
+        if (last_fill[s] > 0) drain_wait(full + 8u * s, (last_fill[s] - 1) / kN & 1);
       for (uint32_t i = (q_loads > 2 ? q_loads - 2 : 0); i < q_loads; ++i)
         drain_wait(bar_q_full + 8u * (i & 1u), (i >> 1) & 1);
     }
@@ -416,7 +496,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
     if (leader) umma_commit(bar_mma_done);
     __syncwarp();
     drain_wait(bar_mma_done, 0);
-  } else {
+  } else if (!KV8 || warp < 6) {
     // ---------------------------------------------------------- softmax + epilogue
     const int quarter = warp & 3;            // TMEM lane quarter of this warp
     const int r = quarter * 32 + lane;       // tile row (S^T) / channel (O^T)
@@ -636,7 +716,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
           // denominator when the call has one
           float inv_l, lse_v;
           finish_row(mcol[c], L, p.sinks ? p.sinks[qh] : -INFINITY, inv_l, lse_v);
-          const float v = o[c] * inv_l;
+          const float v = o[c] * (inv_l * p.out_scale);   // fp8 V factor (1 otherwise)
           if (p.rounding == 3) static_cast<float*>(p.out)[row * kD + r] = v;
           else static_cast<uint16_t*>(p.out)[row * kD + r] = round_out<BF16>(v, p.rounding);
           if (r == 0 && p.lse) p.lse[row] = lse_v;
@@ -644,6 +724,57 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
       }
     }
     tc_fence_before();
+  } else {
+    // ---------------------------------------------------------- fp8 converters
+    // Warps 6-9 (fp8 caches only): thread t widens row t of each staging
+    // tile (128 E4M3 codes, exact in bf16 / fp16) into ring tile `fills %
+    // kSlots` in the MMA's 128-byte-swizzled layout: K as [channel half][row],
+    // V as [16-row group][channel half][row % 16].  Fills alternate K, V.
+    if constexpr (KV8) {
+      const int t = threadIdx.x - 6 * 32;
+      const uint32_t sw = (uint32_t)(t & 7);   // swizzle phase of the row (same on both sides)
+      uint32_t seen = 0, fills = 0;
+      bool ok = true;
+      for (;;) {
+        const uint32_t rs = seen % kItemRing;
+        if (!mbar_wait(bar_item_full + 8u * rs, (seen / kItemRing) & 1, abort_flag)) break;
+        const ItemEntry e = items[rs];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_item_empty + 8u * rs);
+        ++seen;
+        if (e.b < 0) break;
+        const int n_fills = 2 * ((e.k1 - e.k0 + KT - 1) / KT);
+        for (int f = 0; f < n_fills; ++f, ++fills) {
+          const uint32_t s8 = fills % kStages, sr = fills % kSlots;
+          if (!mbar_wait(bar_st_full + 8u * s8, (fills / kStages) & 1, abort_flag)) { ok = false; break; }
+          if (fills >= kSlots &&
+              !mbar_wait(bar_kv_empty + 8u * sr, ((fills / kSlots) - 1) & 1, abort_flag)) {
+            ok = false;
+            break;
+          }
+          const uint8_t* src = smem + kStageOff + s8 * kStage8Bytes + t * 128;
+          uint8_t* dst = smem + kRingOff + sr * kTileBytes;
+          const bool is_v = (fills & 1u) != 0;
+          uint8_t* row0 = is_v ? dst + (t >> 4) * 4096 + (t & 15) * 128 : dst + t * 128;
+          const int half_stride = is_v ? 2048 : kHalfBytes;
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const uint4 w = *reinterpret_cast<const uint4*>(src + ((c ^ sw) << 4));
+            uint4 lo, hi;
+            widen_e4m3x16<BF16>(w, lo, hi);
+            uint8_t* hrow = row0 + (c >> 2) * half_stride;
+            const uint32_t c0 = 2u * (c & 3);
+            *reinterpret_cast<uint4*>(hrow + ((c0 ^ sw) << 4)) = lo;
+            *reinterpret_cast<uint4*>(hrow + (((c0 + 1u) ^ sw) << 4)) = hi;
+          }
+          // every thread publishes its own row to the tensor core's proxy
+          fence_proxy_async_smem();
+          mbar_arrive(bar_st_empty + 8u * s8);
+          mbar_arrive(bar_kv_full + 8u * sr);
+        }
+        if (!ok) break;
+      }
+    }
   }
 
   __syncthreads();
@@ -654,13 +785,19 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
   if (threadIdx.x == 0 && *abort_flag) report_status(p.status, kStatusTimeout);
 }
 
+template <bool BF16, int GH, bool KV8>
+cudaError_t launch_k(const DecodeParams& p, int grid, cudaStream_t stream) {
+  using L = Lay<KV8>;
+  static std::atomic<uint64_t> smem_set{0};
+  const cudaError_t e = ensure_dynamic_smem(decode_tc_kernel<BF16, GH, KV8>, L::kSmemBytes, smem_set);
+  if (e != cudaSuccess) return e;
+  decode_tc_kernel<BF16, GH, KV8><<<grid, L::kThreads, L::kSmemBytes, stream>>>(p);
+  return cudaGetLastError();
+}
+
 template <bool BF16, int GH>
 cudaError_t launch_t(const DecodeParams& p, int grid, cudaStream_t stream) {
-  static std::atomic<uint64_t> smem_set{0};
-  const cudaError_t e = ensure_dynamic_smem(decode_tc_kernel<BF16, GH>, kSmemBytes, smem_set);
-  if (e != cudaSuccess) return e;
-  decode_tc_kernel<BF16, GH><<<grid, kThreads, kSmemBytes, stream>>>(p);
-  return cudaGetLastError();
+  return p.kv_fp8 ? launch_k<BF16, GH, true>(p, grid, stream) : launch_k<BF16, GH, false>(p, grid, stream);
 }
 
 template <bool BF16>

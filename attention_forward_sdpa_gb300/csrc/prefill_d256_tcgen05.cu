@@ -445,6 +445,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_d256_kernel(const __grid_
     const int64_t tok = (int64_t)q_begin + row0 + r;
     float inv_l, lse_v;
     finish_row(m, l, FEAT && p.sinks ? p.sinks[head] : -INFINITY, inv_l, lse_v);
+    if (FEAT) inv_l *= p.out_scale;   // fp8 V factor (1 otherwise)
     // The Q buffer is free once o_full has fired (it covers every product
     // that read Q); the epilogue stages its output there.
     if (rows == kBM && p.rounding != 3) {
@@ -573,7 +574,8 @@ cudaError_t launch_d256(const PrefillParams& p, dim3 grid, cudaStream_t stream) 
 }  // namespace
 
 cudaError_t launch_prefill_d256(const PrefillParams& p, bool bf16, dim3 grid, cudaStream_t stream) {
-  const bool feat = p.win_left >= 0 || p.win_right >= 0 || p.score_xform || p.sinks;
+  const bool feat = p.win_left >= 0 || p.win_right >= 0 || p.score_xform || p.sinks ||
+                    p.out_scale != 1.f;
   if (feat) return bf16 ? launch_d256<true, true>(p, grid, stream) : launch_d256<false, true>(p, grid, stream);
   return bf16 ? launch_d256<true, false>(p, grid, stream) : launch_d256<false, false>(p, grid, stream);
 }

@@ -488,6 +488,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     const int64_t tok = (int64_t)q_begin + t_row0 + r;
     float inv_l, lse_v;
     finish_row(m, l, FEAT && p.sinks ? p.sinks[t_head] : -INFINITY, inv_l, lse_v);
+    if (FEAT) inv_l *= p.out_scale;   // fp8 V factor (1 otherwise)
     if (t_rows == kBM && p.rounding != 3) {
       // Full tile, 16-bit output: the rows are written into this tile's Q
       // slot (free: the o_full commit covers every product that read it) in
@@ -625,7 +626,8 @@ cudaError_t launch_one_f(const PrefillParams& p, dim3 grid, cudaStream_t stream)
 
 template <int D, bool BF16>
 cudaError_t launch_one(const PrefillParams& p, dim3 grid, cudaStream_t stream) {
-  const bool feat = p.win_left >= 0 || p.win_right >= 0 || p.score_xform || p.sinks;
+  const bool feat = p.win_left >= 0 || p.win_right >= 0 || p.score_xform || p.sinks ||
+                    p.out_scale != 1.f;
   return feat ? launch_one_f<D, BF16, true>(p, grid, stream) : launch_one_f<D, BF16, false>(p, grid, stream);
 }
 

@@ -108,11 +108,17 @@ FEATURE_WORKLOADS = {
     "decode_bf16_b64_paged16_softcap_alibi_sinks": ("decode_bf16_b64_paged16",
                                                     {"softcap": 30.0, "alibi": True,
                                                      "sinks": True}),
+    # fp8 E4M3 caches (per-tensor factors): the same draws, stored as codes
+    "decode_bf16_b64_paged16_fp8kv": ("decode_bf16_b64_paged16", {"kv_fp8": True}),
+    "prefill_chunked_bf16_b4_fp8kv": ("prefill_chunked_bf16_b4", {"kv_fp8": True}),
+    "prefill_causal_bf16_gqa_s2048_fp8kv": ("prefill_causal_bf16_gqa_s2048", {"kv_fp8": True}),
 }
 
 
-def feature_args(recipe: dict, num_q_heads: int, dev) -> dict:
+def feature_args(recipe: dict, num_q_heads: int, dev, prob=None) -> dict:
     out = {}
+    if recipe.get("kv_fp8"):
+        out["kv_scales"] = (prob.k_scale, prob.v_scale)
     if "window" in recipe:
         out["window"] = recipe["window"]
     if "softcap" in recipe:
@@ -128,10 +134,12 @@ def feature_args(recipe: dict, num_q_heads: int, dev) -> dict:
 
 def decode_bytes(prob, window=(-1, -1)) -> float:
     """K + V bytes of the visible keys (a left window keeps the last
-    left + 1 keys of each sequence) plus Q and O."""
+    left + 1 keys of each sequence; fp8 caches hold one byte per element)
+    plus Q and O."""
     el = 2
+    kv_el = 1 if getattr(prob, "kv_fp8", False) else 2
     keys = [min(k, window[0] + 1) if window[0] >= 0 else k for k in prob.kv_lens]
-    kv = 2.0 * sum(keys) * prob.num_kv_heads * prob.head_size * el
+    kv = 2.0 * sum(keys) * prob.num_kv_heads * prob.head_size * kv_el
     qo = 2.0 * prob.num_seqs * prob.num_q_heads * prob.head_size * el
     return kv + qo
 
@@ -601,8 +609,15 @@ def run_sweep(args, dev):
              else list(attn_inputs.WORKLOADS) + list(FEATURE_WORKLOADS))
     for name in names:
         base, recipe = FEATURE_WORKLOADS.get(name, (name, {}))
-        prob = attn_inputs.workload(base)
-        feat = feature_args(recipe, prob.num_q_heads, dev)
+        prob = (attn_inputs.workload(base, kv_dtype=torch.float8_e4m3fn) if recipe.get("kv_fp8")
+                else attn_inputs.workload(base))
+        feat = feature_args(recipe, prob.num_q_heads, dev, prob)
+        if recipe.get("kv_fp8") and prob.max_seqlen_q > 1:
+            feat["fp8_workspace"] = torch.empty(
+                attn.attn_fp8_prefill_workspace_size(prob.num_seqs, prob.max_seqlen_k,
+                                                     prob.num_kv_heads, prob.head_size,
+                                                     prob.block_size),
+                dtype=torch.uint8, device=dev)
         window = recipe.get("window", (-1, -1))
         t = device_args(prob, dev)
         out = torch.empty_like(t["q"])

@@ -220,10 +220,12 @@ attn_status_t attn_fwd_decode(void* out, const void* q, const void* k_cache, con
  *                O = sum_j e^(s_j) V_j / (sum_j e^(s_j) + e^(z_h)); the
  *                log-sum-exp output includes it (z_h for a row with no
  *                visible key, whose output is 0).
- * Passing NULL for the whole struct, or {-1, -1, 0, NULL, NULL}, is the plain
- * call.  Errors: window values below -1, a softcap that is negative or not
- * finite, or per-head arrays that are not 4-byte aligned give
- * ATTN_ERR_INVALID_ARG.  The struct is read during the call only; the
+ * Passing NULL for the whole struct, or {-1, -1, 0, NULL, NULL} with the
+ * remaining fields zero, is the plain call.  Errors: window values below -1,
+ * a softcap that is negative or not finite, per-head arrays that are not
+ * 4-byte aligned, kv_fp8 outside {0, 1} or fp8 factors that are not finite
+ * and positive give ATTN_ERR_INVALID_ARG; a missing or short fp8 prefill
+ * workspace gives ATTN_ERR_WORKSPACE.  The struct is read during the call only; the
  * device arrays must stay valid until the work on `stream` has run.
  */
 typedef struct {
@@ -232,7 +234,31 @@ typedef struct {
   float softcap;
   const float* alibi_slopes;
   const float* sinks;
+  /* fp8 K/V caches ([ALG] sec. 9 lists fp8 among the flags without defining
+   * it; this library takes the common convention).  kv_fp8 = 1: k_cache and
+   * v_cache hold OCP E4M3 codes (1 byte per element, same [num_blocks,
+   * block_size, Hkv, d] layout, 16-byte aligned) and the key and value meant
+   * are k_scale * code and v_scale * code; q and out keep `dtype`.  kv_fp8 = 0
+   * ignores the four fields below.  k_scale and v_scale must be finite and
+   * > 0.  Decode reads the codes in its kernels.  Prefill first widens the
+   * pages each sequence references into `workspace` (device memory of at
+   * least attn_fp8_prefill_workspace_size() bytes, 256-byte aligned, owned
+   * by the caller and not touched after the work on `stream` has run), then
+   * runs the 16-bit kernels on that copy; the dense entry point does not
+   * take fp8 (ATTN_ERR_UNSUPPORTED). */
+  int32_t kv_fp8;
+  float k_scale;
+  float v_scale;
+  void* workspace;
+  size_t workspace_bytes;
 } attn_features_t;
+
+/* Bytes of `workspace` an fp8 prefill call needs: two 16-bit caches of
+ * num_seqs * ceil(max_seqlen_k / block_size) pages plus their block table.
+ * 0 for invalid arguments. */
+size_t attn_fp8_prefill_workspace_size(int32_t num_seqs, int32_t max_seqlen_k,
+                                       int32_t num_kv_heads, int32_t head_size,
+                                       int32_t block_size);
 
 /* attn_fwd_prefill, attn_fwd_dense and attn_fwd_decode with feature flags
  * (the other arguments as for those calls).  Decode keeps its kernel choice:
@@ -314,7 +340,8 @@ attn_status_t attn_round_f32(void* out, const float* in, int64_t n, attn_dtype_t
 /* Human-readable name of a status code (static string). */
 const char* attn_status_string(attn_status_t status);
 
-/* ABI version of this header (incremented on incompatible changes). */
+/* ABI version of this header (incremented on incompatible changes; 2 added
+ * the fp8 fields of attn_features_t). */
 int32_t attn_abi_version(void);
 
 #ifdef __cplusplus

@@ -55,7 +55,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_status_strings_and_version(lib):
-    assert lib.attn_abi_version() == 1
+    assert lib.attn_abi_version() == 2
     for code in range(7):
         assert lib.attn_status_string(code)
     assert lib.attn_status_string(99) == b"unknown status"
@@ -249,3 +249,44 @@ def test_binding_refuses_cpu_tensors(lib):
     with pytest.raises(TypeError):
         attn.prefill(q.float(), k, k, bt, torch.tensor([0, 4], dtype=torch.int32),
                      torch.tensor([4], dtype=torch.int32), max_seqlen_q=4, max_seqlen_k=4)
+
+
+def fp8_feat(pkg, kv_fp8=1, k_scale=0.5, v_scale=2.0, ws=None, ws_bytes=0):
+    return pkg._Features(-1, -1, 0.0, None, None, kv_fp8, k_scale, v_scale, ws, ws_bytes)
+
+
+@pytest.mark.parametrize("kv_fp8,k_scale,v_scale", [
+    (2, 1.0, 1.0), (-1, 1.0, 1.0),                 # flag outside {0, 1}
+    (1, 0.0, 1.0), (1, -1.0, 1.0),                 # factors not positive
+    (1, 1.0, float("nan")), (1, float("inf"), 1.0),
+])
+def test_fp8_fields_are_validated(lib, kv_fp8, k_scale, v_scale):
+    import attention_forward_sdpa_gb300 as pkg
+    pkg.load_library()
+    P = ctypes.POINTER(pkg._Features)
+    f = fp8_feat(pkg, kv_fp8, k_scale, v_scale, FAKE, 1 << 30)
+    assert lib.attn_fwd_prefill_ex(*prefill_args(), ctypes.cast(ctypes.byref(f), P)) == 1
+    assert lib.attn_fwd_decode_ex(*decode_args(), ctypes.cast(ctypes.byref(f), P)) == 1
+
+
+def test_fp8_prefill_needs_its_workspace_and_dense_refuses_fp8(lib):
+    import attention_forward_sdpa_gb300 as pkg
+    pkg.load_library()
+    P = ctypes.POINTER(pkg._Features)
+    need = lib.attn_fp8_prefill_workspace_size(2, 200, 2, 128, 64)
+    for ws, nbytes in ((None, 0), (FAKE, need - 1), (ctypes.c_void_p(0x10010), need)):
+        f = fp8_feat(pkg, ws=ws, ws_bytes=nbytes)   # missing, short, misaligned
+        assert lib.attn_fwd_prefill_ex(*prefill_args(), ctypes.cast(ctypes.byref(f), P)) == 4
+    qs = (ctypes.c_int64 * 3)(4096, 1024, 128)
+    f = fp8_feat(pkg, ws=FAKE, ws_bytes=need)
+    assert lib.attn_fwd_dense_ex(FAKE, FAKE, FAKE, FAKE, qs, qs, qs, qs, 2, 32, 16, 8, 2, 128,
+                                 0.088, 1, 1, 0, None, None, None,
+                                 ctypes.cast(ctypes.byref(f), P)) == 2
+
+
+def test_fp8_prefill_workspace_size_is_arithmetic(lib):
+    # 2 sequences x ceil(200 / 64) = 4 pages of 64 x 2 x 128 elements, two
+    # 16-bit copies (K, V), then the 8-entry block table rounded up to 256 bytes
+    assert lib.attn_fp8_prefill_workspace_size(2, 200, 2, 128, 64) == 2 * 8 * 16384 * 2 + 256
+    assert lib.attn_fp8_prefill_workspace_size(0, 200, 2, 128, 64) == 0
+    assert lib.attn_fp8_prefill_workspace_size(1, 0, 1, 64, 16) == 2 * 1024 * 2 + 256
