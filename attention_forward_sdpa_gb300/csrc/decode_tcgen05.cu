@@ -37,6 +37,7 @@
 // softmax warps also goes through an mbarrier so that it is bounded.
 
 #include "attn_internal.h"
+#include "e4m3.cuh"
 #include "round16.cuh"
 #include "score_features.cuh"
 #include "sm103_ptx.cuh"
@@ -101,33 +102,6 @@ constexpr uint32_t kTmemCols = 64;      // S^T x 2 (16 columns each), O^T (16)
 constexpr uint32_t kOCol = 32u;
 
 __device__ __forceinline__ uint32_t s_col(uint32_t g) { return (g & 1u) ? 16u : 0u; }
-
-// Two E4M3 codes (low byte -> low half) to two 16-bit values of the query
-// format.  E4M3 -> f16x2 is exact in hardware; f16 -> f32 -> bf16 is exact
-// for these values (at most 4 significant bits).
-template <bool BF16>
-__device__ __forceinline__ uint32_t widen_e4m3x2(uint32_t two_codes) {
-  uint32_t h;
-  const uint16_t c = (uint16_t)two_codes;
-  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"(c));
-  if constexpr (!BF16) return h;
-  const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h));
-  const __nv_bfloat162 b = __floats2bfloat162_rn(f.x, f.y);
-  return *reinterpret_cast<const uint32_t*>(&b);
-}
-
-// 16 codes -> 16 values in element order (lo: codes 0-7, hi: codes 8-15)
-template <bool BF16>
-__device__ __forceinline__ void widen_e4m3x16(const uint4 w, uint4& lo, uint4& hi) {
-  lo.x = widen_e4m3x2<BF16>(w.x);
-  lo.y = widen_e4m3x2<BF16>(w.x >> 16);
-  lo.z = widen_e4m3x2<BF16>(w.y);
-  lo.w = widen_e4m3x2<BF16>(w.y >> 16);
-  hi.x = widen_e4m3x2<BF16>(w.z);
-  hi.y = widen_e4m3x2<BF16>(w.z >> 16);
-  hi.z = widen_e4m3x2<BF16>(w.w);
-  hi.w = widen_e4m3x2<BF16>(w.w >> 16);
-}
 
 __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
   const uint64_t t0 = global_timer_ns();
@@ -761,7 +735,7 @@ __global__ void __launch_bounds__(Lay<KV8>::kThreads, 1) decode_tc_kernel(const 
           for (int c = 0; c < 8; ++c) {
             const uint4 w = *reinterpret_cast<const uint4*>(src + ((c ^ sw) << 4));
             uint4 lo, hi;
-            widen_e4m3x16<BF16>(w, lo, hi);
+            e4m3x16_widen<BF16>(w, lo, hi);
             uint8_t* hrow = row0 + (c >> 2) * half_stride;
             const uint32_t c0 = 2u * (c & 3);
             *reinterpret_cast<uint4*>(hrow + ((c0 ^ sw) << 4)) = lo;
