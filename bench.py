@@ -64,8 +64,8 @@ CSRC = os.path.join(ROOT, "attention_forward_sdpa_gb300", "csrc")
 # edit of comments alone keeps it; the ncu summaries under profiles/ record
 # each capture).
 MEASURED_TRAFFIC = {
-    "prefill": ("prefill_tcgen05.cu", "b7b90a6bcd729b89", 25.241088e6 + 512.0),
-    "decode": ("decode_tcgen05.cu", "6d3a0c8a3e4abc34", 1.130830e9 + 9.613056e6),
+    "prefill": ("prefill_tcgen05.cu", "d9fef89a07482736", 25.240576e6 + 256.0),
+    "decode": ("decode_tcgen05.cu", "d6b7df528e0f7095", 1.130839e9 + 9.729024e6),
 }
 
 
