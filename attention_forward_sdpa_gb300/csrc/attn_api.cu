@@ -203,7 +203,9 @@ int decode_prepare_and_launch(DecodeParams& p, int head_size, bool bf16, void* w
   }
   const int G = p.num_q_heads / p.num_kv_heads;
   const bool pow2 = (G & (G - 1)) == 0;
-  const bool tc_path = head_size == 128 && ((G <= 16 && pow2) || G % 16 == 0);
+  // tcgen05 kernel: head size 128, or 64 with 16-bit caches
+  const bool tc_path = (head_size == 128 || (head_size == 64 && !p.kv_fp8)) &&
+                       ((G <= 16 && pow2) || G % 16 == 0);
   if (!tc_path) {
     cudaError_t e = launch_decode(p, head_size, bf16, G, stream);
     return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
@@ -256,10 +258,10 @@ int decode_prepare_and_launch(DecodeParams& p, int head_size, bool bf16, void* w
   if (!p.kv_fp8) {
     // V as (channel in half, slot, channel half, head, page): one box brings
     // both channel halves of 16 slots x F heads
-    const cuuint64_t dims[5] = {64, (cuuint64_t)p.block_size, 2, (cuuint64_t)p.num_kv_heads,
+    const cuuint64_t dims[5] = {64, (cuuint64_t)p.block_size, d / 64, (cuuint64_t)p.num_kv_heads,
                                 (cuuint64_t)p.num_blocks};
     const cuuint64_t strides[4] = {slot_stride, 128, d * 2, block_stride};
-    const cuuint32_t box[5] = {64, 16, 2, (cuuint32_t)p.kv_per_item, 1};
+    const cuuint32_t box[5] = {64, 16, (cuuint32_t)(d / 64), (cuuint32_t)p.kv_per_item, 1};
     if (!encode_tiled(&p.tm_v, bf16, 5, dims, strides, box, p.v_cache, CU_TENSOR_MAP_SWIZZLE_128B))
       return ATTN_ERR_CUDA;
   }
@@ -267,7 +269,7 @@ int decode_prepare_and_launch(DecodeParams& p, int head_size, bool bf16, void* w
   if (sms <= 0) return ATTN_ERR_CUDA;
   const int grid = (int)(n_items < sms ? n_items : sms);
   if (cudaMemsetAsync(p.counter, 0, counter_bytes, stream) != cudaSuccess) return ATTN_ERR_CUDA;
-  cudaError_t e = launch_decode_tc(p, bf16, grid, stream);
+  cudaError_t e = launch_decode_tc(p, head_size, bf16, grid, stream);
   if (e == cudaSuccess && p.num_splits > 1) e = launch_decode_combine(p, head_size, bf16, stream);
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }

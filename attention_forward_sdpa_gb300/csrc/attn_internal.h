@@ -106,7 +106,8 @@ cudaError_t launch_prefill(const PrefillParams& p, int head_size, bool bf16, dim
 cudaError_t launch_prefill_d256(const PrefillParams& p, bool bf16, dim3 grid, cudaStream_t stream);
 cudaError_t launch_decode(const DecodeParams& p, int head_size, bool bf16, int group,
                           cudaStream_t stream);
-cudaError_t launch_decode_tc(const DecodeParams& p, bool bf16, int grid, cudaStream_t stream);
+cudaError_t launch_decode_tc(const DecodeParams& p, int head_size, bool bf16, int grid,
+                             cudaStream_t stream);
 cudaError_t launch_decode_combine(const DecodeParams& p, int head_size, bool bf16,
                                   cudaStream_t stream);
 

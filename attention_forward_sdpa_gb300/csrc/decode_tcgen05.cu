@@ -45,12 +45,9 @@
 namespace attn {
 namespace {
 
-constexpr int kD = 128;                 // head size handled here
 constexpr int kRows = 128;              // tile rows: 16-key boxes x F heads x 16 keys
 constexpr int kItemRing = 4;
-constexpr int kTileBytes = kRows * kD * 2;      // 32 KB
-constexpr int kHalfBytes = kRows * 128;         // K: 128 rows x 64 channels
-constexpr int kQBytes = 2 * 16 * 128;           // two channel halves of [16 heads][64]
+constexpr int kHalfBytes = kRows * 128;         // K: 128 rows x 64 channels (one channel half)
 constexpr int kPBytes = 2 * 16 * 128;           // two row halves of [16 heads][64 rows]
 constexpr int kSeqCache = 2048;                 // cached sequence lengths
 constexpr int kSortMax = 128;                   // longest-first order up to this many sequences
@@ -68,16 +65,23 @@ struct ItemEntry {
   int sk;      // the sequence's KV length (its decode row is aligned with key sk - 1)
 };
 
-constexpr int kStage8Bytes = kRows * kD;       // an fp8 tile: 128 rows x 128 codes (16 KB)
+constexpr int kStage8Bytes = kRows * 128;      // an fp8 tile: 128 rows x 128 codes (16 KB)
 
 // Shared-memory layout.  With 16-bit caches the ring holds six tiles.  With
 // fp8 caches (KV8) TMA lands the codes in four 16 KB staging tiles, four
 // converter warps widen them into a ring of four 16-bit tiles (the layout
 // the MMAs read), and the CTA has 320 threads instead of 192.
-template <bool KV8>
+template <int D, bool KV8>
 struct Lay {
+  static_assert((D == 128 || D == 64) && (!KV8 || D == 128), "head size 128, or 64 with 16-bit caches");
+  static constexpr int kD = D;
+  static constexpr int kHalves = D / 64;                 // 64-channel halves of a row
+  static constexpr int kTileBytes = kRows * D * 2;       // 32 KB (d = 128), 16 KB (d = 64)
+  static constexpr int kQBytes = kHalves * 16 * 128;     // channel halves of [16 heads][64]
+  static constexpr int kVGroup = kHalves * 2048;         // V: one 16-row group, all halves
   static constexpr int kThreads = KV8 ? 320 : 192;
-  static constexpr int kSlots = KV8 ? 4 : 6;     // 16-bit K/V ring slots of one tile each
+  // 16-bit K/V ring slots of one tile each (the same bytes in flight at d = 64)
+  static constexpr int kSlots = KV8 ? 4 : (D == 64 ? 12 : 6);
   static constexpr int kStages = KV8 ? 4 : 0;    // fp8 staging slots
   static constexpr int kRingOff = 0;
   static constexpr int kStageOff = kRingOff + kSlots * kTileBytes;
@@ -127,9 +131,11 @@ __device__ __forceinline__ uint32_t p_offset(int q, int r) {
   return (uint32_t)(half * 2048 + q * 128 + chunk * 16 + (c & 7) * 2);
 }
 
-template <bool BF16, int GH, bool KV8>
-__global__ void __launch_bounds__(Lay<KV8>::kThreads, 1) decode_tc_kernel(const __grid_constant__ DecodeParams p) {
-  using L = Lay<KV8>;
+template <bool BF16, int GH, bool KV8, int D>
+__global__ void __launch_bounds__(Lay<D, KV8>::kThreads, 1) decode_tc_kernel(const __grid_constant__ DecodeParams p) {
+  using L = Lay<D, KV8>;
+  constexpr int kD = L::kD, kHalves = L::kHalves, kTileBytes = L::kTileBytes;
+  constexpr int kQBytes = L::kQBytes, kVGroup = L::kVGroup;
   constexpr int kThreads = L::kThreads, kSlots = L::kSlots, kStages = L::kStages;
   constexpr int kRingOff = L::kRingOff, kStageOff = L::kStageOff, kQOff = L::kQOff;
   constexpr int kPOff = L::kPOff, kRedOff = L::kRedOff, kLRedOff = L::kLRedOff;
@@ -312,8 +318,8 @@ __global__ void __launch_bounds__(Lay<KV8>::kThreads, 1) decode_tc_kernel(const 
       if (q_loads >= 2 && !mbar_wait(bar_q_empty + 8u * qs, ((q_loads >> 1) - 1) & 1, abort_flag))
         break;
       if (lane == 0) {
-        mbar_arrive_expect_tx(bar_q_full + 8u * qs, (uint32_t)(2 * p.q_box_rows * 128));
-        for (int h = 0; h < 2; ++h)
+        mbar_arrive_expect_tx(bar_q_full + 8u * qs, (uint32_t)(kHalves * p.q_box_rows * 128));
+        for (int h = 0; h < kHalves; ++h)
           tma_load_3d(sQ + qs * kQBytes + h * 2048, &p.tm_q, bar_q_full + 8u * qs, h * 64, q0, b);
       }
       ++q_loads;
@@ -358,7 +364,7 @@ __global__ void __launch_bounds__(Lay<KV8>::kThreads, 1) decode_tc_kernel(const 
               break;
             }
             const uint32_t bar = bar_kv_full + 8u * s;
-            if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)(nbox * F * 4096));
+            if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)(nbox * F * kVGroup));
             __syncwarp();
             if (mine) {
               const uint32_t slot = sRing + s * kTileBytes;
@@ -366,10 +372,10 @@ __global__ void __launch_bounds__(Lay<KV8>::kThreads, 1) decode_tc_kernel(const 
                 // K: [channel half][tile row], box j -> rows [16 F j, 16 F (j + 1))
                 const uint32_t dst = slot + j * F * 16 * 128;
                 tma_load_4d(dst, &p.tm_k, bar, 0, row, kvh0, page);
-                tma_load_4d(dst + kHalfBytes, &p.tm_k, bar, 64, row, kvh0, page);
+                if (kHalves == 2) tma_load_4d(dst + kHalfBytes, &p.tm_k, bar, 64, row, kvh0, page);
               } else {
                 // V: [16-row group][channel half][16 rows], both halves at once
-                tma_load_5d(slot + j * F * 4096, &p.tm_v, bar, 0, row, 0, kvh0, page);
+                tma_load_5d(slot + j * F * kVGroup, &p.tm_v, bar, 0, row, 0, kvh0, page);
               }
             }
             last_fill[s] = fills + 1;
@@ -408,8 +414,11 @@ __global__ void __launch_bounds__(Lay<KV8>::kThreads, 1) decode_tc_kernel(const 
         const uint32_t b0 = sP + (pend_g & 1u) * kPBytes;
 #pragma unroll
         for (int kk = 0; kk < kRows / 16; ++kk) {
-          // A = V^T (MN-major): 16 rows per step, channel halves 2048 B apart
-          umma_ss(tmem + kOCol, make_sdesc_sw128(a0 + kk * 4096, 2048, 1024),
+          // A = V^T (MN-major): 16 rows per step, channel halves 2048 B apart.
+          // At d = 64 the product still has M = 128: its rows 64-127 read the
+          // next 16-row group (finite or not), land in O^T rows that are
+          // never stored, and never touch rows 0-63.
+          umma_ss(tmem + kOCol, make_sdesc_sw128(a0 + kk * kVGroup, 2048, 1024),
                   make_sdesc_sw128(b0 + (kk >> 2) * 2048 + (kk & 3) * 32, 16, 1024), idesc_pv,
                   (pend_first && kk == 0) ? 0u : 1u);
         }
@@ -628,11 +637,11 @@ __global__ void __launch_bounds__(Lay<KV8>::kThreads, 1) decode_tc_kernel(const 
           const uint32_t fill_v = 2u * g + 1u;
           const uint32_t sv_slot = fill_v % kSlots;
           if (!mbar_wait(bar_kv_full + 8u * sv_slot, (fill_v / kSlots) & 1, abort_flag)) { ok = false; break; }
-          uint8_t* vrow = smem + (sRing - base) + sv_slot * kTileBytes + grp16 * 4096 + (r & 15) * 128;
+          uint8_t* vrow = smem + (sRing - base) + sv_slot * kTileBytes + grp16 * kVGroup + (r & 15) * 128;
 #pragma unroll
           for (int c = 0; c < 8; ++c) {
             *reinterpret_cast<uint4*>(vrow + c * 16) = make_uint4(0u, 0u, 0u, 0u);
-            *reinterpret_cast<uint4*>(vrow + 2048 + c * 16) = make_uint4(0u, 0u, 0u, 0u);
+            if (kHalves == 2) *reinterpret_cast<uint4*>(vrow + 2048 + c * 16) = make_uint4(0u, 0u, 0u, 0u);
           }
         }
         uint8_t* pb = smem + (sP - base) + (g & 1u) * kPBytes;
@@ -680,7 +689,7 @@ __global__ void __launch_bounds__(Lay<KV8>::kThreads, 1) decode_tc_kernel(const 
         const int qh = (e.kvh0 + hh) * G + (e.q0 - e.kvh0 * G) + jj;
         const int64_t row = (int64_t)e.b * Hq + qh;
         if (p.num_splits > 1) {
-          p.part_o[(row * p.num_splits + e.split) * kD + r] = o[c];
+          if (r < kD) p.part_o[(row * p.num_splits + e.split) * kD + r] = o[c];
           if (r == 0) {
             p.part_ml[(row * p.num_splits + e.split) * 2 + 0] = mcol[c];
             p.part_ml[(row * p.num_splits + e.split) * 2 + 1] = L;
@@ -691,8 +700,10 @@ __global__ void __launch_bounds__(Lay<KV8>::kThreads, 1) decode_tc_kernel(const 
           float inv_l, lse_v;
           finish_row(mcol[c], L, p.sinks ? p.sinks[qh] : -INFINITY, inv_l, lse_v);
           const float v = o[c] * (inv_l * p.out_scale);   // fp8 V factor (1 otherwise)
-          if (p.rounding == 3) static_cast<float*>(p.out)[row * kD + r] = v;
-          else static_cast<uint16_t*>(p.out)[row * kD + r] = round_out<BF16>(v, p.rounding);
+          if (r < kD) {   // O^T rows past the head size are not part of the result
+            if (p.rounding == 3) static_cast<float*>(p.out)[row * kD + r] = v;
+            else static_cast<uint16_t*>(p.out)[row * kD + r] = round_out<BF16>(v, p.rounding);
+          }
           if (r == 0 && p.lse) p.lse[row] = lse_v;
         }
       }
@@ -759,29 +770,34 @@ __global__ void __launch_bounds__(Lay<KV8>::kThreads, 1) decode_tc_kernel(const 
   if (threadIdx.x == 0 && *abort_flag) report_status(p.status, kStatusTimeout);
 }
 
-template <bool BF16, int GH, bool KV8>
+template <bool BF16, int GH, bool KV8, int D>
 cudaError_t launch_k(const DecodeParams& p, int grid, cudaStream_t stream) {
-  using L = Lay<KV8>;
+  using L = Lay<D, KV8>;
   static std::atomic<uint64_t> smem_set{0};
-  const cudaError_t e = ensure_dynamic_smem(decode_tc_kernel<BF16, GH, KV8>, L::kSmemBytes, smem_set);
+  const cudaError_t e = ensure_dynamic_smem(decode_tc_kernel<BF16, GH, KV8, D>, L::kSmemBytes, smem_set);
   if (e != cudaSuccess) return e;
-  decode_tc_kernel<BF16, GH, KV8><<<grid, L::kThreads, L::kSmemBytes, stream>>>(p);
+  decode_tc_kernel<BF16, GH, KV8, D><<<grid, L::kThreads, L::kSmemBytes, stream>>>(p);
   return cudaGetLastError();
 }
 
 template <bool BF16, int GH>
-cudaError_t launch_t(const DecodeParams& p, int grid, cudaStream_t stream) {
-  return p.kv_fp8 ? launch_k<BF16, GH, true>(p, grid, stream) : launch_k<BF16, GH, false>(p, grid, stream);
+cudaError_t launch_t(const DecodeParams& p, int head_size, int grid, cudaStream_t stream) {
+  if (head_size == 64) {
+    if (p.kv_fp8) return cudaErrorInvalidValue;   // fp8 at d = 64 takes the SIMT kernel
+    return launch_k<BF16, GH, false, 64>(p, grid, stream);
+  }
+  return p.kv_fp8 ? launch_k<BF16, GH, true, 128>(p, grid, stream)
+                  : launch_k<BF16, GH, false, 128>(p, grid, stream);
 }
 
 template <bool BF16>
-cudaError_t launch_b(const DecodeParams& p, int grid, cudaStream_t stream) {
+cudaError_t launch_b(const DecodeParams& p, int head_size, int grid, cudaStream_t stream) {
   switch (p.heads_per_item) {
-    case 1: return launch_t<BF16, 1>(p, grid, stream);
-    case 2: return launch_t<BF16, 2>(p, grid, stream);
-    case 4: return launch_t<BF16, 4>(p, grid, stream);
-    case 8: return launch_t<BF16, 8>(p, grid, stream);
-    case 16: return launch_t<BF16, 16>(p, grid, stream);
+    case 1: return launch_t<BF16, 1>(p, head_size, grid, stream);
+    case 2: return launch_t<BF16, 2>(p, head_size, grid, stream);
+    case 4: return launch_t<BF16, 4>(p, head_size, grid, stream);
+    case 8: return launch_t<BF16, 8>(p, head_size, grid, stream);
+    case 16: return launch_t<BF16, 16>(p, head_size, grid, stream);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -793,8 +809,9 @@ cudaError_t launch_b(const DecodeParams& p, int grid, cudaStream_t stream) {
 // when G is a multiple of 16 above it; a power of two) and kv_per_item (F,
 // with F * heads_per_item <= 16 and F dividing num_kv_heads), encoded the
 // tensor maps and zeroed p.counter on `stream`.
-cudaError_t launch_decode_tc(const DecodeParams& p, bool bf16, int grid, cudaStream_t stream) {
-  return bf16 ? launch_b<true>(p, grid, stream) : launch_b<false>(p, grid, stream);
+cudaError_t launch_decode_tc(const DecodeParams& p, int head_size, bool bf16, int grid,
+                             cudaStream_t stream) {
+  return bf16 ? launch_b<true>(p, head_size, grid, stream) : launch_b<false>(p, head_size, grid, stream);
 }
 
 }  // namespace attn

@@ -191,6 +191,7 @@ def workload(name: str, seed: int = 0, **over) -> PagedProblem:
                                      d=128, one page per sequence, N(0,1)
       prefill_causal_bf16_gqa_s2048_d256   the 2048 workload at head size 256
       prefill_causal_bf16_s8192_d256       the 8192 workload at head size 256
+      decode_bf16_b64_paged16_d64 / _d256  the decode workload at head size 64 / 256
     Keyword overrides replace any argument of paged_problem (e.g. smaller
     lengths for parity runs at reduced size)."""
     if name == "prefill_causal_fp16_s128_d64":
@@ -214,8 +215,11 @@ def workload(name: str, seed: int = 0, **over) -> PagedProblem:
         kw = dict(q_lens=[16384] * 4, kv_lens=[16384] * 4, num_q_heads=16, num_kv_heads=16,
                   head_size=128, block_size=16384, dtype=torch.bfloat16, sigma=1.0, causal=False,
                   permute=False, poison=False)
-    elif name in ("prefill_causal_bf16_gqa_s2048_d256", "prefill_causal_bf16_s8192_d256"):
+    elif name in ("prefill_causal_bf16_gqa_s2048_d256", "prefill_causal_bf16_s8192_d256",
+                  "decode_bf16_b64_paged16_d256"):
         return workload(name[:-len("_d256")], seed=seed, **{"head_size": 256, **over})
+    elif name == "decode_bf16_b64_paged16_d64":
+        return workload("decode_bf16_b64_paged16", seed=seed, **{"head_size": 64, **over})
     else:
         raise KeyError(name)
     kw.update(over)
@@ -225,4 +229,5 @@ def workload(name: str, seed: int = 0, **over) -> PagedProblem:
 WORKLOADS = ("prefill_causal_fp16_s128_d64", "prefill_causal_bf16_gqa_s2048",
              "decode_bf16_b64_paged16", "prefill_causal_bf16_s8192",
              "prefill_chunked_bf16_b4", "dense_bf16_bshd_s16384",
-             "prefill_causal_bf16_gqa_s2048_d256", "prefill_causal_bf16_s8192_d256")
+             "prefill_causal_bf16_gqa_s2048_d256", "prefill_causal_bf16_s8192_d256",
+             "decode_bf16_b64_paged16_d64", "decode_bf16_b64_paged16_d256")
