@@ -38,7 +38,8 @@ from .build_ext import LIB_PATH
 __all__ = ["attn_fwd_prefill", "attn_fwd_dense", "attn_fwd_decode", "attn_fwd_decode_noalloc",
            "has_features", "dense",
            "attn_decode_workspace_size", "attn_fp8_prefill_workspace_size",
-           "attn_round_f32", "attn_status_string", "attn_abi_version", "prefill", "decode",
+           "attn_round_f32", "attn_status_string", "attn_abi_version", "attn_tensor_map_cache_stats",
+           "prefill", "decode",
            "AttnError", "library_path", "load_library", "RTNE", "RTNA", "RTZ", "OUT_F32"]
 
 ATTN_OK = 0
@@ -110,6 +111,8 @@ def load_library() -> ctypes.CDLL:
         lib.attn_status_string.argtypes = [ctypes.c_int]
         lib.attn_abi_version.restype = i32
         lib.attn_abi_version.argtypes = []
+        lib.attn_tensor_map_cache_stats.restype = None
+        lib.attn_tensor_map_cache_stats.argtypes = [P, P]
         _lib = lib
         return lib
 
@@ -213,6 +216,13 @@ def _cache_dev(t, name, q_dtype, kv_scales):
 
 def attn_abi_version() -> int:
     return int(load_library().attn_abi_version())
+
+
+def attn_tensor_map_cache_stats() -> tuple:
+    """(hits, misses) of the library's tensor-map cache."""
+    h, m = ctypes.c_uint64(0), ctypes.c_uint64(0)
+    load_library().attn_tensor_map_cache_stats(ctypes.byref(h), ctypes.byref(m))
+    return int(h.value), int(m.value)
 
 
 def attn_status_string(status: int) -> str:

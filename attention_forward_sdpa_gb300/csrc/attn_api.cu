@@ -150,27 +150,110 @@ void prefill_grid(int head_size, bool pair_heads, int num_q_heads, int64_t row_b
 
 namespace attn {
 
-bool encode_tiled(CUtensorMap* map, bool bf16, int rank, const cuuint64_t* dims,
-                  const cuuint64_t* strides_bytes, const cuuint32_t* box, const void* base,
-                  CUtensorMapSwizzle swz) {
+namespace {
+
+// Tensor-map cache.  A CUtensorMap is a pure function of the arguments of
+// cuTensorMapEncodeTiled (base address, element type, sizes, strides, box,
+// swizzle), so an entry keyed on all of them stays valid for as long as the
+// process runs, whatever happened to the memory in between: a buffer freed and
+// allocated again at the same address with the same shape encodes to the same
+// map.  The cache saves the host-side encode of repeated calls (a serving
+// loop calls with the same cache pool and, usually, the same activation
+// buffers).  4-way set associative with LRU replacement (64 sets), so the
+// four descriptors of one call never evict one another; one mutex.
+struct MapKey {
+  const void* base;
+  uint32_t dtype, rank, swz, pad;
+  cuuint64_t dims[5];
+  cuuint64_t strides[4];
+  cuuint32_t box[5];
+  uint32_t pad2;
+};
+
+struct MapEntry {
+  bool valid;
+  uint64_t used;     // last use (a global tick), for LRU replacement
+  MapKey key;
+  CUtensorMap map;
+};
+
+constexpr int kMapSets = 64, kMapWays = 4;
+std::mutex g_map_mutex;
+MapEntry g_map_cache[kMapSets][kMapWays];
+uint64_t g_map_tick = 0;
+std::atomic<uint64_t> g_map_hits{0}, g_map_misses{0};
+
+uint64_t key_hash(const MapKey& k) {
+  // FNV-1a over the key's bytes
+  const unsigned char* b = reinterpret_cast<const unsigned char*>(&k);
+  uint64_t h = 1469598103934665603ull;
+  for (size_t i = 0; i < sizeof(MapKey); ++i) h = (h ^ b[i]) * 1099511628211ull;
+  return h;
+}
+
+bool encode_cached(CUtensorMap* map, CUtensorMapDataType dtype, int rank, const cuuint64_t* dims,
+                   const cuuint64_t* strides_bytes, const cuuint32_t* box, const void* base,
+                   CUtensorMapSwizzle swz) {
+  if (rank < 1 || rank > 5) return false;
+  MapKey k;
+  std::memset(&k, 0, sizeof(k));
+  k.base = base;
+  k.dtype = (uint32_t)dtype;
+  k.rank = (uint32_t)rank;
+  k.swz = (uint32_t)swz;
+  for (int i = 0; i < rank; ++i) {
+    k.dims[i] = dims[i];
+    k.box[i] = box[i];
+    if (i + 1 < rank) k.strides[i] = strides_bytes[i];
+  }
+  MapEntry* set = g_map_cache[key_hash(k) % kMapSets];
+  {
+    std::lock_guard<std::mutex> lock(g_map_mutex);
+    for (int w = 0; w < kMapWays; ++w) {
+      MapEntry& e = set[w];
+      if (e.valid && std::memcmp(&e.key, &k, sizeof(k)) == 0) {
+        e.used = ++g_map_tick;
+        *map = e.map;
+        g_map_hits.fetch_add(1, std::memory_order_relaxed);
+        return true;
+      }
+    }
+  }
   EncodeTiledFn fn = get_encode_fn();
   if (!fn) return false;
   cuuint32_t estr[5] = {1, 1, 1, 1, 1};
-  return fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
-            (cuuint32_t)rank, const_cast<void*>(base), dims, strides_bytes, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  if (fn(map, dtype, (cuuint32_t)rank, const_cast<void*>(base), dims, strides_bytes, box, estr,
+         CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return false;
+  g_map_misses.fetch_add(1, std::memory_order_relaxed);
+  std::lock_guard<std::mutex> lock(g_map_mutex);
+  int victim = 0;
+  for (int w = 0; w < kMapWays; ++w) {
+    if (!set[w].valid) { victim = w; break; }
+    if (set[w].used < set[victim].used) victim = w;
+  }
+  MapEntry& e = set[victim];
+  e.valid = true;
+  e.used = ++g_map_tick;
+  e.key = k;
+  e.map = *map;
+  return true;
+}
+
+}  // namespace
+
+bool encode_tiled(CUtensorMap* map, bool bf16, int rank, const cuuint64_t* dims,
+                  const cuuint64_t* strides_bytes, const cuuint32_t* box, const void* base,
+                  CUtensorMapSwizzle swz) {
+  return encode_cached(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                       rank, dims, strides_bytes, box, base, swz);
 }
 
 bool encode_tiled_u8(CUtensorMap* map, int rank, const cuuint64_t* dims,
                      const cuuint64_t* strides_bytes, const cuuint32_t* box, const void* base,
                      CUtensorMapSwizzle swz) {
-  EncodeTiledFn fn = get_encode_fn();
-  if (!fn) return false;
-  cuuint32_t estr[5] = {1, 1, 1, 1, 1};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, (cuuint32_t)rank, const_cast<void*>(base), dims,
-            strides_bytes, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return encode_cached(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, rank, dims, strides_bytes, box, base, swz);
 }
 
 int device_sm_count() {
@@ -279,6 +362,11 @@ int decode_prepare_and_launch(DecodeParams& p, int head_size, bool bf16, void* w
 extern "C" {
 
 int32_t attn_abi_version(void) { return 2; }
+
+void attn_tensor_map_cache_stats(uint64_t* hits, uint64_t* misses) {
+  if (hits) *hits = attn::g_map_hits.load(std::memory_order_relaxed);
+  if (misses) *misses = attn::g_map_misses.load(std::memory_order_relaxed);
+}
 
 const char* attn_status_string(attn_status_t s) {
   switch (s) {

@@ -340,6 +340,14 @@ attn_status_t attn_round_f32(void* out, const float* in, int64_t n, attn_dtype_t
 /* Human-readable name of a status code (static string). */
 const char* attn_status_string(attn_status_t status);
 
+/* Counters of the library's tensor-map cache (process-wide): hits are
+ * encodes served from the cache, misses are encodes done by the driver.  The
+ * TMA descriptors each call needs are cached on everything that defines them
+ * (address, element type, sizes, strides, box, swizzle), so a repeated call on
+ * the same buffers does no driver encode.  Either pointer may be NULL.
+ * Diagnostic only; there is no counterpart in the pages. */
+void attn_tensor_map_cache_stats(uint64_t* hits, uint64_t* misses);
+
 /* ABI version of this header (incremented on incompatible changes; 2 added
  * the fp8 fields of attn_features_t). */
 int32_t attn_abi_version(void);
