@@ -540,9 +540,52 @@ def time_oracle(prob, rows, threads):
     oracle.sdpa(prob.q, prob.k_cache, prob.v_cache, prob.block_table, prob.query_start_loc,
                 prob.seq_lens, num_q_heads=prob.num_q_heads, num_kv_heads=prob.num_kv_heads,
                 head_size=prob.head_size, block_size=prob.block_size, scale=prob.scale,
-                causal=prob.causal, dtype=oracle.BF16, rows=rows, n_threads=threads,
-                want_lse=False)
+                causal=prob.causal,
+                dtype=oracle.BF16 if prob.dtype == torch.bfloat16 else oracle.F16, rows=rows,
+                n_threads=threads, want_lse=False)
     return time.perf_counter() - t0
+
+
+# (workload, rows: "full" or a sample size, threads: "all" or 1)
+CPU_SWEEP_PLAN = (
+    ("prefill_causal_fp16_s128_d64", "full", "all"),
+    ("prefill_causal_fp16_s128_d64", "full", 1),
+    ("prefill_causal_bf16_gqa_s2048", "full", "all"),
+    ("prefill_causal_bf16_gqa_s2048", 4096, 1),
+    ("decode_bf16_b64_paged16", "full", "all"),
+    ("prefill_chunked_bf16_b4", "full", "all"),
+    ("prefill_causal_bf16_s8192", 16384, "all"),
+    ("dense_bf16_bshd_s16384", 2048, "all"),
+)
+
+
+def run_cpu_sweep(args):
+    """The fp64 oracle timed on the host cores for every measured workload:
+    in full where that takes up to a couple of minutes (C1, C2, C3, C4b),
+    else on a random row sample whose time is extrapolated to the workload
+    by its FLOPs (labelled so); C1 and C2 also single-threaded.  One JSON
+    line per entry.  A baseline, not a target."""
+    import platform
+    cores = os.cpu_count() or 1
+    cpu = platform.processor() or platform.machine()
+    for name, rows, th in CPU_SWEEP_PLAN:
+        prob = attn_inputs.workload(name)
+        threads = cores if th == "all" else int(th)
+        total = prob.total_q * prob.num_q_heads
+        full = rows == "full"
+        r = np.arange(total, dtype=np.int64) if full else oracle_sample(prob, int(rows), 11)
+        secs = time_oracle(prob, r, threads)
+        if prob.max_seqlen_q == 1:
+            work, unit = oracle_bytes(prob, r), "GB/s"
+            value, whole = work / secs / 1e9, decode_bytes(prob)
+        else:
+            work, unit = oracle_cost(prob, r), "TFLOP/s"
+            value, whole = work / secs / 1e12, prefill_flops(prob)
+        print(json.dumps({"workload": name, "kind": "oracle", "threads": threads, "cpu": cpu,
+                          "rows": int(len(r)), "rows_total": int(total), "seconds": secs,
+                          "value": value, "unit": unit, "extrapolated": not full,
+                          "workload_seconds": secs if full else secs * whole / max(work, 1.0)}),
+              flush=True)
 
 
 def cpu_baseline(pp, dp, seconds):
@@ -762,6 +805,8 @@ def main():
     ap.add_argument("--no-graph", action="store_true", help="skip the CUDA-graph replay timings")
     ap.add_argument("--cpu-seconds", type=float, default=16.0)
     ap.add_argument("--ref-rows", type=int, default=128)
+    ap.add_argument("--cpu-sweep", action="store_true",
+                    help="time the fp64 oracle on the host cores for every measured workload")
     ap.add_argument("--sweep", nargs="?", const="all", default=None,
                     help="time each named workload (comma-separated names, default all)")
     args = ap.parse_args()
@@ -773,6 +818,10 @@ def main():
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if args.impl == "reference":
         run_reference(args, rank, world)
+        return
+    if args.cpu_sweep:
+        if rank == 0:
+            run_cpu_sweep(args)
         return
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
