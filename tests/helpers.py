@@ -80,3 +80,41 @@ def worst(got_rows, ref, n=5):
     flat = np.argsort(d, axis=None)[::-1][:n]
     return [(int(i // d.shape[1]), int(i % d.shape[1]), float(got_rows.flat[i]), float(ref.flat[i]))
             for i in flat]
+
+
+# ----------------------------------------------------------------------------
+# parity report: per checked case, max |err|, mean |err| and the largest error
+# in units of the output format's spacing at the reference value (ULP)
+# ----------------------------------------------------------------------------
+
+PARITY = []
+_MANT = {torch.bfloat16: 7, torch.float16: 10}
+_MIN_EXP = {torch.bfloat16: -126, torch.float16: -14}
+
+
+def ulp_of(ref: np.ndarray, dtype) -> np.ndarray:
+    """Spacing of the 16-bit format at |ref| (its subnormal spacing below the
+    smallest normal)."""
+    a = np.abs(ref)
+    e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+    e = np.maximum(e, _MIN_EXP[dtype])
+    return np.exp2(e - _MANT[dtype])
+
+
+ULP_FLOOR = 2.0 ** -6   # below this |ref| the absolute error is the meaningful one
+
+
+def record(name: str, got: np.ndarray, ref: np.ndarray, dtype) -> dict:
+    """ULP counts are taken where |ref| >= ULP_FLOOR (near zero the format's
+    spacing is far finer than the fp32 accumulation error, and the absolute
+    error is reported instead); p99.9 is over those elements."""
+    d = np.abs(got - ref)
+    fin = np.isfinite(ref)
+    big = fin & (np.abs(ref) >= ULP_FLOOR)
+    u = d[big] / ulp_of(ref[big], dtype) if big.any() else np.zeros(1)
+    row = {"case": name, "elements": int(got.size),
+           "max_abs": float(d[fin].max()) if fin.any() else 0.0,
+           "mean_abs": float(d[fin].mean()) if fin.any() else 0.0,
+           "max_ulp": float(u.max()), "p999_ulp": float(np.percentile(u, 99.9))}
+    PARITY.append(row)
+    return row

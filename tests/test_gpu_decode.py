@@ -13,23 +13,31 @@ import pytest
 import torch
 
 import attn_inputs
-from tests.helpers import TOL, as_rows, gpu_decode, gpu_prefill, max_err, oracle_run, to_dev, worst
+from tests.helpers import (TOL, as_rows, gpu_decode, gpu_prefill, max_err, oracle_run, record,
+                           to_dev, worst)
 
 pytestmark = pytest.mark.gpu
 
 
-def check(prob, splits=8, **kw):
+def check(prob, splits=8, name=None, **kw):
     out = gpu_decode(prob, splits=splits, **kw)
     torch.cuda.synchronize()
     ref, _ = oracle_run(prob)
     got = as_rows(out)
+    if name:
+        record(name, got, ref, prob.dtype)
     err = max_err(got, ref)
     assert err <= TOL[prob.dtype], (err, worst(got, ref))
     return out
 
 
 def test_workload_decode_full():
-    check(attn_inputs.workload("decode_bf16_b64_paged16"), splits=8)
+    check(attn_inputs.workload("decode_bf16_b64_paged16"), splits=8, name="decode_bf16_b64_paged16")
+
+
+@pytest.mark.parametrize("name", ["decode_bf16_b64_paged16_d64", "decode_bf16_b64_paged16_d256"])
+def test_workload_decode_other_head_sizes(name):
+    check(attn_inputs.workload(name), splits=8, name=name)
 
 
 @pytest.mark.parametrize("hq,hkv", [(8, 8), (8, 4), (8, 2), (16, 2), (24, 2), (12, 4), (16, 1),
