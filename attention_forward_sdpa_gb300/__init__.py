@@ -293,18 +293,23 @@ def _strides3(t, name):
 
 def attn_fwd_dense(out, q, k, v, *, scale: float, causal: bool, rounding: int = RTNE, lse=None,
                    status=None, stream=None, window=None, softcap: float = 0.0,
-                   alibi_slopes=None, sinks=None) -> None:
+                   alibi_slopes=None, sinks=None, kv_scales=None, fp8_workspace=None) -> None:
     """Calls attn_fwd_dense on logical [batch, seq, heads, head_size] CUDA
     tensors in any (batch, seq, head) stride order: BSHD tensors as they are,
     BHSD tensors x as x.transpose(1, 2) (a view, nothing is copied)."""
     lib = load_library()
     dt = _dtype_code(q.dtype)
-    for t, name, want in ((q, "q", None), (k, "k", q.dtype), (v, "v", q.dtype),
+    kv_want = None if kv_scales is not None else q.dtype
+    for t, name, want in ((q, "q", None), (k, "k", kv_want), (v, "v", kv_want),
                           (out, "out", torch.float32 if rounding == OUT_F32 else q.dtype)):
         if not isinstance(t, torch.Tensor) or not t.is_cuda:
             raise ValueError(f"{name} must be a CUDA tensor")
         if want is not None and t.dtype != want:
             raise TypeError(f"{name} must be {want}, got {t.dtype}")
+    if kv_scales is not None:
+        for t, name in ((k, "k"), (v, "v")):
+            if t.dtype not in _FP8_CACHE_DTYPES:
+                raise TypeError(f"{name} must be torch.float8_e4m3fn or uint8 with kv_scales")
     if lse is not None:
         _dev(lse, "lse", torch.float32)
     if status is not None:
@@ -318,7 +323,7 @@ def attn_fwd_dense(out, q, k, v, *, scale: float, causal: bool, rounding: int = 
     args = (_ptr(out), _ptr(q), _ptr(k), _ptr(v), qs, ks, vs, os_, b, sq, sk, hq, hkv, d,
             float(scale), int(bool(causal)), dt, int(rounding), _ptr(lse), _ptr(status),
             _stream_handle(stream))
-    feat = _features(hq, window, softcap, alibi_slopes, sinks)
+    feat = _features(hq, window, softcap, alibi_slopes, sinks, kv_scales, fp8_workspace)
     if feat is None:
         _check(lib.attn_fwd_dense(*args), "attn_fwd_dense")
     else:
@@ -453,6 +458,12 @@ def dense(q, k, v, *, layout: str = "bshd", scale: float | None = None, causal: 
     qv = view(q)
     lse = (torch.empty((qv.shape[0], qv.shape[2], qv.shape[1]), dtype=torch.float32,
                        device=q.device) if return_lse else None)
+    if features.get("kv_scales") is not None and features.get("fp8_workspace") is None:
+        kv = view(k)
+        nbytes = attn_fp8_prefill_workspace_size(kv.shape[0], kv.shape[1], kv.shape[2],
+                                                 kv.shape[3], max(kv.shape[1], 1))
+        features = dict(features, fp8_workspace=torch.empty(max(nbytes, 1), dtype=torch.uint8,
+                                                            device=q.device))
     attn_fwd_dense(view(out), qv, view(k), view(v), scale=scale, causal=causal, rounding=rounding,
                    lse=lse, status=status, stream=stream, **features)
     return (out, lse) if return_lse else out

@@ -572,7 +572,6 @@ attn_status_t attn_fwd_dense_ex(void* out, const void* q, const void* k, const v
   // ---- host-side validation (no CUDA call before this block ends)
   Features feat;
   if (read_features(features, feat) != ATTN_OK) return ATTN_ERR_INVALID_ARG;
-  if (feat.kv_fp8) return ATTN_ERR_UNSUPPORTED;   // fp8 caches: paged prefill and decode only
   if (batch < 0 || seqlen_q < 0 || seqlen_k < 0) return ATTN_ERR_INVALID_ARG;
   if (num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0) return ATTN_ERR_INVALID_ARG;
   if (dtype != ATTN_F16 && dtype != ATTN_BF16) return ATTN_ERR_INVALID_ARG;
@@ -585,12 +584,26 @@ attn_status_t attn_fwd_dense_ex(void* out, const void* q, const void* k, const v
   if (!out || !q || !k || !v) return ATTN_ERR_INVALID_ARG;
   if (!aligned16(out) || !aligned16(q) || !aligned16(k) || !aligned16(v)) return ATTN_ERR_INVALID_ARG;
   const int64_t out_elem = rounding == ATTN_OUT_F32 ? 4 : 2;
+  const int64_t kv_elem = feat.kv_fp8 ? 1 : 2;     // fp8: one byte per element
   for (int i = 0; i < 3; ++i) {
     // positive strides whose byte sizes are multiples of 16 (TMA and 16-byte stores)
     if (q_strides[i] <= 0 || k_strides[i] <= 0 || v_strides[i] <= 0 || o_strides[i] <= 0) return ATTN_ERR_INVALID_ARG;
-    if ((q_strides[i] * 2) % 16 || (k_strides[i] * 2) % 16 || (v_strides[i] * 2) % 16 ||
+    if ((q_strides[i] * 2) % 16 || (k_strides[i] * kv_elem) % 16 || (v_strides[i] * kv_elem) % 16 ||
         (o_strides[i] * out_elem) % 16)
       return ATTN_ERR_INVALID_ARG;
+  }
+  // fp8: K and V are widened into the workspace (the layout of an fp8
+  // prefill over `batch` sequences with one page of seqlen_k rows each)
+  const float scale_eff = feat.kv_fp8 ? scale * feat.k_scale : scale;
+  if (!valid_scale(scale_eff)) return ATTN_ERR_INVALID_ARG;
+  Fp8Workspace fw;
+  if (feat.kv_fp8) {
+    if (!fp8_workspace_layout(batch, seqlen_k, num_kv_heads, head_size,
+                              seqlen_k > 0 ? seqlen_k : 1, fw))
+      return ATTN_ERR_INVALID_ARG;
+    if (!feat.workspace || feat.workspace_bytes < fw.total ||
+        (reinterpret_cast<uintptr_t>(feat.workspace) & 255u))
+      return ATTN_ERR_WORKSPACE;
   }
   const int group = num_q_heads / num_kv_heads;
   const bool pair_heads = group % 2 == 0;
@@ -602,9 +615,25 @@ attn_status_t attn_fwd_dense_ex(void* out, const void* q, const void* k, const v
   attn_status_t st = check_device();
   if (st != ATTN_OK) return st;
 
+  const bool bf16 = dtype == ATTN_BF16;
+  int64_t dense_kv_strides[3];
+  if (feat.kv_fp8) {
+    uint8_t* ws = static_cast<uint8_t*>(feat.workspace);
+    cudaError_t e = attn::launch_kv_widen_dense(k, v, k_strides, v_strides, batch, seqlen_k,
+                                                num_kv_heads, head_size, bf16, ws + fw.k_off,
+                                                ws + fw.v_off, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return ATTN_ERR_CUDA;
+    k = ws + fw.k_off;
+    v = ws + fw.v_off;
+    dense_kv_strides[0] = (int64_t)seqlen_k * num_kv_heads * head_size;
+    dense_kv_strides[1] = (int64_t)num_kv_heads * head_size;
+    dense_kv_strides[2] = head_size;
+    k_strides = dense_kv_strides;
+    v_strides = dense_kv_strides;
+  }
+
   attn::PrefillParams p;
   std::memset(&p, 0, sizeof(p));
-  const bool bf16 = dtype == ATTN_BF16;
   const cuuint64_t d = (cuuint64_t)head_size;
   const cuuint64_t sk_dim = (cuuint64_t)(seqlen_k > 0 ? seqlen_k : 1);   // never read when 0
   {
@@ -651,9 +680,9 @@ attn_status_t attn_fwd_dense_ex(void* out, const void* q, const void* k, const v
   p.o_stride_h = o_strides[2];
   p.causal = causal;
   p.rounding = (int32_t)rounding;
-  p.scale_log2 = scale * kLog2e;
+  p.scale_log2 = scale_eff * kLog2e;
   p.wait_limit_ns = kDefaultWaitLimitNs;
-  set_features(p, feat, scale);
+  set_features(p, feat, scale_eff);
 
   dim3 grid((unsigned)gx, (unsigned)batch, (unsigned)gz);
   cudaError_t e = attn::launch_prefill(p, head_size, bf16, grid, static_cast<cudaStream_t>(stream));

@@ -157,6 +157,14 @@ cudaError_t launch_kv_widen(const void* k8, const void* v8, const int32_t* block
                             int64_t page_elems, bool bf16, void* k16, void* v16,
                             int32_t* table_out, int32_t* status, cudaStream_t stream);
 
+// fp8 dense: widens logical [B, Sk, Hkv, d] E4M3 K and V with the given
+// (batch, row, head) strides (in bytes, channels contiguous) into contiguous
+// 16-bit [B, Sk, Hkv, d] copies.
+cudaError_t launch_kv_widen_dense(const void* k8, const void* v8, const int64_t* k_strides,
+                                  const int64_t* v_strides, int32_t batch, int32_t seqlen_k,
+                                  int32_t num_kv_heads, int32_t head_size, bool bf16, void* k16,
+                                  void* v16, cudaStream_t stream);
+
 // In-kernel error codes written to the status word (same values as the
 // public attn_status_t).
 enum : int32_t { kStatusBadArg = 1, kStatusBadBlockTable = 5, kStatusTimeout = 6 };

@@ -68,7 +68,70 @@ __global__ void __launch_bounds__(256) kv_widen_kernel(const __grid_constant__ W
   vd[1] = vhi;
 }
 
+// Dense fp8 input: K and V as logical [B, Sk, Hkv, d] E4M3 codes with any
+// (batch, row, head) strides (bytes, multiples of 16; channels contiguous)
+// widened into contiguous 16-bit [B, Sk, Hkv, d] copies.  One thread per 16
+// codes of K and of V.
+struct WidenDenseParams {
+  const uint8_t* k8;
+  const uint8_t* v8;
+  uint16_t* k16;
+  uint16_t* v16;
+  int64_t ks[3], vs[3];   // source strides (elements = bytes): batch, row, head
+  int64_t groups;         // B * Sk * Hkv * d / 16
+  int32_t seqlen_k, num_kv_heads, head_size;
+};
+
+template <bool BF16>
+__global__ void __launch_bounds__(256) kv_widen_dense_kernel(const __grid_constant__ WidenDenseParams p) {
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= p.groups) return;
+  const int per_row = p.head_size / 16;
+  const int64_t row = i / per_row;                 // ((b * Sk) + s) * Hkv + h
+  const int c16 = (int)(i % per_row);
+  const int h = (int)(row % p.num_kv_heads);
+  const int64_t bs = row / p.num_kv_heads;
+  const int s = (int)(bs % p.seqlen_k);
+  const int64_t b = bs / p.seqlen_k;
+  const int64_t ko = b * p.ks[0] + s * p.ks[1] + h * p.ks[2] + 16 * c16;
+  const int64_t vo = b * p.vs[0] + s * p.vs[1] + h * p.vs[2] + 16 * c16;
+  uint4 klo, khi, vlo, vhi;
+  e4m3x16_widen<BF16>(__ldg(reinterpret_cast<const uint4*>(p.k8 + ko)), klo, khi);
+  e4m3x16_widen<BF16>(__ldg(reinterpret_cast<const uint4*>(p.v8 + vo)), vlo, vhi);
+  uint4* kd = reinterpret_cast<uint4*>(p.k16) + 2 * i;
+  uint4* vd = reinterpret_cast<uint4*>(p.v16) + 2 * i;
+  kd[0] = klo;
+  kd[1] = khi;
+  vd[0] = vlo;
+  vd[1] = vhi;
+}
+
 }  // namespace
+
+cudaError_t launch_kv_widen_dense(const void* k8, const void* v8, const int64_t* k_strides,
+                                  const int64_t* v_strides, int32_t batch, int32_t seqlen_k,
+                                  int32_t num_kv_heads, int32_t head_size, bool bf16, void* k16,
+                                  void* v16, cudaStream_t stream) {
+  WidenDenseParams p;
+  p.k8 = static_cast<const uint8_t*>(k8);
+  p.v8 = static_cast<const uint8_t*>(v8);
+  p.k16 = static_cast<uint16_t*>(k16);
+  p.v16 = static_cast<uint16_t*>(v16);
+  for (int i = 0; i < 3; ++i) {
+    p.ks[i] = k_strides[i];
+    p.vs[i] = v_strides[i];
+  }
+  p.seqlen_k = seqlen_k;
+  p.num_kv_heads = num_kv_heads;
+  p.head_size = head_size;
+  p.groups = (int64_t)batch * seqlen_k * num_kv_heads * (head_size / 16);
+  if (p.groups == 0) return cudaSuccess;
+  const int64_t blocks = (p.groups + 255) / 256;
+  if (blocks > 2147483647) return cudaErrorInvalidValue;
+  if (bf16) kv_widen_dense_kernel<true><<<(unsigned)blocks, 256, 0, stream>>>(p);
+  else kv_widen_dense_kernel<false><<<(unsigned)blocks, 256, 0, stream>>>(p);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_kv_widen(const void* k8, const void* v8, const int32_t* block_table,
                             int32_t bt_stride, const int32_t* seq_lens, int32_t num_seqs,

@@ -244,8 +244,10 @@ typedef struct {
    * pages each sequence references into `workspace` (device memory of at
    * least attn_fp8_prefill_workspace_size() bytes, 256-byte aligned, owned
    * by the caller and not touched after the work on `stream` has run), then
-   * runs the 16-bit kernels on that copy; the dense entry point does not
-   * take fp8 (ATTN_ERR_UNSUPPORTED). */
+   * runs the 16-bit kernels on that copy.  The dense entry point takes fp8
+   * K and V ([B, Sk, Hkv, d] codes whose strides, in bytes, are multiples of
+   * 16) the same way, with a workspace of
+   * attn_fp8_prefill_workspace_size(B, Sk, Hkv, d, Sk) bytes. */
   int32_t kv_fp8;
   float k_scale;
   float v_scale;

@@ -269,7 +269,7 @@ def test_fp8_fields_are_validated(lib, kv_fp8, k_scale, v_scale):
     assert lib.attn_fwd_decode_ex(*decode_args(), ctypes.cast(ctypes.byref(f), P)) == 1
 
 
-def test_fp8_prefill_needs_its_workspace_and_dense_refuses_fp8(lib):
+def test_fp8_calls_need_their_workspace(lib):
     import attention_forward_sdpa_gb300 as pkg
     pkg.load_library()
     P = ctypes.POINTER(pkg._Features)
@@ -277,11 +277,22 @@ def test_fp8_prefill_needs_its_workspace_and_dense_refuses_fp8(lib):
     for ws, nbytes in ((None, 0), (FAKE, need - 1), (ctypes.c_void_p(0x10010), need)):
         f = fp8_feat(pkg, ws=ws, ws_bytes=nbytes)   # missing, short, misaligned
         assert lib.attn_fwd_prefill_ex(*prefill_args(), ctypes.cast(ctypes.byref(f), P)) == 4
+    # dense: batch 2, Sq 32, Sk 16, Hq 8, Hkv 2, d 128; its workspace is the
+    # prefill one with one page of Sk rows per batch entry
     qs = (ctypes.c_int64 * 3)(4096, 1024, 128)
-    f = fp8_feat(pkg, ws=FAKE, ws_bytes=need)
-    assert lib.attn_fwd_dense_ex(FAKE, FAKE, FAKE, FAKE, qs, qs, qs, qs, 2, 32, 16, 8, 2, 128,
+    kvs = (ctypes.c_int64 * 3)(16 * 2 * 128, 2 * 128, 128)
+    need_d = lib.attn_fp8_prefill_workspace_size(2, 16, 2, 128, 16)
+    for ws, nbytes in ((None, 0), (FAKE, need_d - 1)):
+        f = fp8_feat(pkg, ws=ws, ws_bytes=nbytes)
+        assert lib.attn_fwd_dense_ex(FAKE, FAKE, FAKE, FAKE, qs, kvs, kvs, qs, 2, 32, 16, 8, 2,
+                                     128, 0.088, 1, 1, 0, None, None, None,
+                                     ctypes.cast(ctypes.byref(f), P)) == 4
+    # fp8 strides are in bytes and must be multiples of 16
+    bad = (ctypes.c_int64 * 3)(16 * 2 * 128, 2 * 128 + 8, 128)
+    f = fp8_feat(pkg, ws=FAKE, ws_bytes=need_d)
+    assert lib.attn_fwd_dense_ex(FAKE, FAKE, FAKE, FAKE, qs, bad, kvs, qs, 2, 32, 16, 8, 2, 128,
                                  0.088, 1, 1, 0, None, None, None,
-                                 ctypes.cast(ctypes.byref(f), P)) == 2
+                                 ctypes.cast(ctypes.byref(f), P)) == 1
 
 
 def test_fp8_prefill_workspace_size_is_arithmetic(lib):

@@ -174,3 +174,37 @@ def test_fp8_prefill_reports_a_bad_page():
                  kv_scales=(prob.k_scale, prob.v_scale))
     torch.cuda.synchronize()
     assert int(status.item()) == 5
+
+
+@pytest.mark.parametrize("layout", ["bshd", "bhsd", "bshd_padded"])
+def test_dense_fp8(layout):
+    """fp8 K/V on the dense strided entry point: against the oracle, and bit
+    for bit against the paged call on the same codes (one page per batch
+    entry)."""
+    import attention_forward_sdpa_gb300 as attn
+    B, Sq, Sk, hq, hkv, d = 2, 200, 384, 8, 2, 128   # Sk: also a valid paged block size
+    prob = attn_inputs.paged_problem(seed=98, q_lens=[Sq] * B, kv_lens=[Sk] * B, num_q_heads=hq,
+                                     num_kv_heads=hkv, head_size=d, block_size=Sk, causal=True,
+                                     permute=False, poison=False, kv_dtype=F8)
+    ks = (prob.k_scale, prob.v_scale)
+    q = prob.q.view(B, Sq, hq, d).cuda()
+    k = prob.k_cache.view(B, Sk, hkv, d).cuda()
+    v = prob.v_cache.view(B, Sk, hkv, d).cuda()
+    lay = "bhsd" if layout == "bhsd" else "bshd"
+    if layout == "bhsd":
+        q, k, v = (x.transpose(1, 2).contiguous() for x in (q, k, v))
+    elif layout == "bshd_padded":
+        def pad(x, extra):
+            big = torch.zeros(*x.shape[:3], x.shape[3] + extra, dtype=x.dtype, device="cuda")
+            big[..., :x.shape[3]] = x
+            return big[..., :x.shape[3]]
+        q, k, v = pad(q, 8), pad(k, 16), pad(v, 32)   # row strides stay 16-byte multiples
+    out = attn.dense(q, k, v, layout=lay, scale=prob.scale, causal=True, kv_scales=ks)
+    torch.cuda.synchronize()
+    packed = (out if lay == "bshd" else out.transpose(1, 2)).contiguous().view(B * Sq, hq, d)
+    ref, _ = oracle_fp8(prob)
+    got = as_rows(packed)
+    assert max_err(got, ref) <= TOL[prob.dtype], worst(got, ref)
+    paged, _ = run_prefill(prob)
+    torch.cuda.synchronize()
+    assert torch.equal(packed.view(torch.int16), paged.view(torch.int16))
