@@ -286,8 +286,8 @@ int decode_prepare_and_launch(DecodeParams& p, int head_size, bool bf16, void* w
   }
   const int G = p.num_q_heads / p.num_kv_heads;
   const bool pow2 = (G & (G - 1)) == 0;
-  // tcgen05 kernel: head size 128, or 64 with 16-bit caches
-  const bool tc_path = (head_size == 128 || (head_size == 64 && !p.kv_fp8)) &&
+  // tcgen05 kernel: head size 128, or 64 / 256 with 16-bit caches
+  const bool tc_path = (head_size == 128 || ((head_size == 64 || head_size == 256) && !p.kv_fp8)) &&
                        ((G <= 16 && pow2) || G % 16 == 0);
   if (!tc_path) {
     cudaError_t e = launch_decode(p, head_size, bf16, G, stream);

@@ -49,7 +49,6 @@ constexpr int kRows = 128;              // tile rows: 16-key boxes x F heads x 1
 constexpr int kItemRing = 4;
 constexpr int kHalfBytes = kRows * 128;         // K: 128 rows x 64 channels (one channel half)
 constexpr int kPBytes = 2 * 16 * 128;           // two row halves of [16 heads][64 rows]
-constexpr int kSeqCache = 2048;                 // cached sequence lengths
 constexpr int kSortMax = 128;                   // longest-first order up to this many sequences
 constexpr float kLn2 = 0.693147180559945309f;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -73,15 +72,19 @@ constexpr int kStage8Bytes = kRows * 128;      // an fp8 tile: 128 rows x 128 co
 // the MMAs read), and the CTA has 320 threads instead of 192.
 template <int D, bool KV8>
 struct Lay {
-  static_assert((D == 128 || D == 64) && (!KV8 || D == 128), "head size 128, or 64 with 16-bit caches");
+  static_assert((D == 128 || D == 64 || D == 256) && (!KV8 || D == 128),
+                "head size 128, or 64 / 256 with 16-bit caches");
   static constexpr int kD = D;
+  static constexpr int kOBlocks = D == 256 ? 2 : 1;      // 128-channel blocks of O^T (TMEM)
+  static constexpr int kSeqCache = D == 256 ? 1024 : 2048;   // cached sequence lengths
   static constexpr int kHalves = D / 64;                 // 64-channel halves of a row
   static constexpr int kTileBytes = kRows * D * 2;       // 32 KB (d = 128), 16 KB (d = 64)
   static constexpr int kQBytes = kHalves * 16 * 128;     // channel halves of [16 heads][64]
   static constexpr int kVGroup = kHalves * 2048;         // V: one 16-row group, all halves
   static constexpr int kThreads = KV8 ? 320 : 192;
-  // 16-bit K/V ring slots of one tile each (the same bytes in flight at d = 64)
-  static constexpr int kSlots = KV8 ? 4 : (D == 64 ? 12 : 6);
+  // 16-bit K/V ring slots of one tile each (about the same bytes in flight
+  // at every head size: 12 x 16 KB, 6 x 32 KB, 3 x 64 KB)
+  static constexpr int kSlots = KV8 ? 4 : (D == 64 ? 12 : (D == 256 ? 3 : 6));
   static constexpr int kStages = KV8 ? 4 : 0;    // fp8 staging slots
   static constexpr int kRingOff = 0;
   static constexpr int kStageOff = kRingOff + kSlots * kTileBytes;
@@ -135,7 +138,8 @@ template <bool BF16, int GH, bool KV8, int D>
 __global__ void __launch_bounds__(Lay<D, KV8>::kThreads, 1) decode_tc_kernel(const __grid_constant__ DecodeParams p) {
   using L = Lay<D, KV8>;
   constexpr int kD = L::kD, kHalves = L::kHalves, kTileBytes = L::kTileBytes;
-  constexpr int kQBytes = L::kQBytes, kVGroup = L::kVGroup;
+  constexpr int kQBytes = L::kQBytes, kVGroup = L::kVGroup, kOBlocks = L::kOBlocks;
+  constexpr int kSeqCache = L::kSeqCache;
   constexpr int kThreads = L::kThreads, kSlots = L::kSlots, kStages = L::kStages;
   constexpr int kRingOff = L::kRingOff, kStageOff = L::kStageOff, kQOff = L::kQOff;
   constexpr int kPOff = L::kPOff, kRedOff = L::kRedOff, kLRedOff = L::kLRedOff;
@@ -371,8 +375,9 @@ __global__ void __launch_bounds__(Lay<D, KV8>::kThreads, 1) decode_tc_kernel(con
               if (kind == 0) {
                 // K: [channel half][tile row], box j -> rows [16 F j, 16 F (j + 1))
                 const uint32_t dst = slot + j * F * 16 * 128;
-                tma_load_4d(dst, &p.tm_k, bar, 0, row, kvh0, page);
-                if (kHalves == 2) tma_load_4d(dst + kHalfBytes, &p.tm_k, bar, 64, row, kvh0, page);
+#pragma unroll
+                for (int h = 0; h < kHalves; ++h)
+                  tma_load_4d(dst + h * kHalfBytes, &p.tm_k, bar, 64 * h, row, kvh0, page);
               } else {
                 // V: [16-row group][channel half][16 rows], both halves at once
                 tma_load_5d(slot + j * F * kVGroup, &p.tm_v, bar, 0, row, 0, kvh0, page);
@@ -413,15 +418,20 @@ __global__ void __launch_bounds__(Lay<D, KV8>::kThreads, 1) decode_tc_kernel(con
         const uint32_t a0 = sRing + sv * kTileBytes;
         const uint32_t b0 = sP + (pend_g & 1u) * kPBytes;
 #pragma unroll
-        for (int kk = 0; kk < kRows / 16; ++kk) {
-          // A = V^T (MN-major): 16 rows per step, channel halves 2048 B apart.
-          // At d = 64 the product still has M = 128: its rows 64-127 read the
-          // next 16-row group (finite or not), land in O^T rows that are
-          // never stored, and never touch rows 0-63.
-          umma_ss(tmem + kOCol, make_sdesc_sw128(a0 + kk * kVGroup, 2048, 1024),
-                  make_sdesc_sw128(b0 + (kk >> 2) * 2048 + (kk & 3) * 32, 16, 1024), idesc_pv,
-                  (pend_first && kk == 0) ? 0u : 1u);
-        }
+        for (int ob = 0; ob < kOBlocks; ++ob)
+#pragma unroll
+          for (int kk = 0; kk < kRows / 16; ++kk) {
+            // A = V^T (MN-major): 16 rows per step, channel halves 2048 B
+            // apart; O^T block ob (channels 128 ob .. 128 ob + 127, TMEM
+            // columns kOCol + 16 ob) starts at channel half 2 ob.  At d = 64
+            // the product still has M = 128: its rows 64-127 read the next
+            // 16-row group (finite or not), land in O^T rows that are never
+            // stored, and never touch rows 0-63.
+            umma_ss(tmem + kOCol + 16u * ob,
+                    make_sdesc_sw128(a0 + kk * kVGroup + ob * 4096, 2048, 1024),
+                    make_sdesc_sw128(b0 + (kk >> 2) * 2048 + (kk & 3) * 32, 16, 1024), idesc_pv,
+                    (pend_first && kk == 0) ? 0u : 1u);
+          }
         umma_commit(bar_pv_done);
         umma_commit(bar_kv_empty + 8u * sv);
       }
@@ -623,12 +633,15 @@ __global__ void __launch_bounds__(Lay<D, KV8>::kThreads, 1) decode_tc_kernel(con
           tc_fence_after();
         }
         if (t > 0 && heavy && rescale) {
-          uint32_t ov[16];
-          tmem_ld16(tmem + lane_off + kOCol, ov);
-          tmem_ld_wait_n<16>(ov);
 #pragma unroll
-          for (int c = 0; c < 16; ++c) ov[c] = __float_as_uint(__uint_as_float(ov[c]) * alpha_all[c]);
-          tmem_st16(tmem + lane_off + kOCol, ov);
+          for (int ob = 0; ob < kOBlocks; ++ob) {
+            uint32_t ov[16];
+            tmem_ld16(tmem + lane_off + kOCol + 16u * ob, ov);
+            tmem_ld_wait_n<16>(ov);
+#pragma unroll
+            for (int c = 0; c < 16; ++c) ov[c] = __float_as_uint(__uint_as_float(ov[c]) * alpha_all[c]);
+            tmem_st16(tmem + lane_off + kOCol + 16u * ob, ov);
+          }
           tmem_st_wait();
         }
         if (!valid) {
@@ -639,10 +652,10 @@ __global__ void __launch_bounds__(Lay<D, KV8>::kThreads, 1) decode_tc_kernel(con
           if (!mbar_wait(bar_kv_full + 8u * sv_slot, (fill_v / kSlots) & 1, abort_flag)) { ok = false; break; }
           uint8_t* vrow = smem + (sRing - base) + sv_slot * kTileBytes + grp16 * kVGroup + (r & 15) * 128;
 #pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            *reinterpret_cast<uint4*>(vrow + c * 16) = make_uint4(0u, 0u, 0u, 0u);
-            if (kHalves == 2) *reinterpret_cast<uint4*>(vrow + 2048 + c * 16) = make_uint4(0u, 0u, 0u, 0u);
-          }
+          for (int h = 0; h < kHalves; ++h)
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+              *reinterpret_cast<uint4*>(vrow + h * 2048 + c * 16) = make_uint4(0u, 0u, 0u, 0u);
         }
         uint8_t* pb = smem + (sP - base) + (g & 1u) * kPBytes;
 #pragma unroll
@@ -658,18 +671,23 @@ __global__ void __launch_bounds__(Lay<D, KV8>::kThreads, 1) decode_tc_kernel(con
       }
       if (!ok) break;
       // ---- item epilogue: denominators, then partial or final output
-      float o[16];
+      float o[kOBlocks][16];   // O^T rows r and (d = 256) r + 128
       if (n_tiles > 0) {
         if (!mbar_wait(bar_pv_done, (g - 1) & 1, abort_flag)) { ok = false; break; }
         tc_fence_after();
-        uint32_t ov[16];
-        tmem_ld16(tmem + lane_off + kOCol, ov);
-        tmem_ld_wait_n<16>(ov);
 #pragma unroll
-        for (int c = 0; c < 16; ++c) o[c] = __uint_as_float(ov[c]);
+        for (int ob = 0; ob < kOBlocks; ++ob) {
+          uint32_t ov[16];
+          tmem_ld16(tmem + lane_off + kOCol + 16u * ob, ov);
+          tmem_ld_wait_n<16>(ov);
+#pragma unroll
+          for (int c = 0; c < 16; ++c) o[ob][c] = __uint_as_float(ov[c]);
+        }
       } else {
 #pragma unroll
-        for (int c = 0; c < 16; ++c) o[c] = 0.f;
+        for (int ob = 0; ob < kOBlocks; ++ob)
+#pragma unroll
+          for (int c = 0; c < 16; ++c) o[ob][c] = 0.f;
       }
       float* lb = lred + (red_uses & 1u) * 128;
 #pragma unroll
@@ -689,7 +707,9 @@ __global__ void __launch_bounds__(Lay<D, KV8>::kThreads, 1) decode_tc_kernel(con
         const int qh = (e.kvh0 + hh) * G + (e.q0 - e.kvh0 * G) + jj;
         const int64_t row = (int64_t)e.b * Hq + qh;
         if (p.num_splits > 1) {
-          if (r < kD) p.part_o[(row * p.num_splits + e.split) * kD + r] = o[c];
+#pragma unroll
+          for (int ob = 0; ob < kOBlocks; ++ob)
+            if (r + 128 * ob < kD) p.part_o[(row * p.num_splits + e.split) * kD + r + 128 * ob] = o[ob][c];
           if (r == 0) {
             p.part_ml[(row * p.num_splits + e.split) * 2 + 0] = mcol[c];
             p.part_ml[(row * p.num_splits + e.split) * 2 + 1] = L;
@@ -699,10 +719,14 @@ __global__ void __launch_bounds__(Lay<D, KV8>::kThreads, 1) decode_tc_kernel(con
           // denominator when the call has one
           float inv_l, lse_v;
           finish_row(mcol[c], L, p.sinks ? p.sinks[qh] : -INFINITY, inv_l, lse_v);
-          const float v = o[c] * (inv_l * p.out_scale);   // fp8 V factor (1 otherwise)
-          if (r < kD) {   // O^T rows past the head size are not part of the result
-            if (p.rounding == 3) static_cast<float*>(p.out)[row * kD + r] = v;
-            else static_cast<uint16_t*>(p.out)[row * kD + r] = round_out<BF16>(v, p.rounding);
+#pragma unroll
+          for (int ob = 0; ob < kOBlocks; ++ob) {
+            const int ch = r + 128 * ob;
+            const float v = o[ob][c] * (inv_l * p.out_scale);   // fp8 V factor (1 otherwise)
+            if (ch < kD) {   // O^T rows past the head size are not part of the result
+              if (p.rounding == 3) static_cast<float*>(p.out)[row * kD + ch] = v;
+              else static_cast<uint16_t*>(p.out)[row * kD + ch] = round_out<BF16>(v, p.rounding);
+            }
           }
           if (r == 0 && p.lse) p.lse[row] = lse_v;
         }
@@ -782,9 +806,10 @@ cudaError_t launch_k(const DecodeParams& p, int grid, cudaStream_t stream) {
 
 template <bool BF16, int GH>
 cudaError_t launch_t(const DecodeParams& p, int head_size, int grid, cudaStream_t stream) {
-  if (head_size == 64) {
-    if (p.kv_fp8) return cudaErrorInvalidValue;   // fp8 at d = 64 takes the SIMT kernel
-    return launch_k<BF16, GH, false, 64>(p, grid, stream);
+  if (head_size == 64 || head_size == 256) {
+    if (p.kv_fp8) return cudaErrorInvalidValue;   // fp8 at d = 64 / 256 takes the SIMT kernel
+    return head_size == 64 ? launch_k<BF16, GH, false, 64>(p, grid, stream)
+                           : launch_k<BF16, GH, false, 256>(p, grid, stream);
   }
   return p.kv_fp8 ? launch_k<BF16, GH, true, 128>(p, grid, stream)
                   : launch_k<BF16, GH, false, 128>(p, grid, stream);
