@@ -1,9 +1,10 @@
 // attn_api.cu -- the extern "C" boundary declared in include/attn_fwd.h:
 // argument validation (all on the host, before any launch), device check,
-// TMA descriptor encoding and grid sizing for attn_fwd_prefill,
-// attn_fwd_dense, attn_fwd_decode and the timeout test hook.  Every compute
-// step runs in the kernels of prefill_tcgen05.cu, decode_tcgen05.cu and
-// decode_splitkv.cu.
+// TMA descriptor encoding (through a cache of descriptors) and grid sizing for
+// attn_fwd_prefill, attn_fwd_dense, attn_fwd_decode, their feature-flagged
+// (_ex) forms and the timeout test hook.  Every compute step runs in the
+// kernels of prefill_tcgen05.cu, prefill_d256_tcgen05.cu, decode_tcgen05.cu,
+// decode_splitkv.cu and kv_widen.cu.
 
 #include <cuda.h>
 #include <cuda_runtime.h>

@@ -17,8 +17,8 @@
 // are merged in a fixed order at the end.
 //
 // This SIMT kernel serves the shapes the tcgen05 decode (decode_tcgen05.cu)
-// does not take: head size 64 and group sizes that are neither a power of two
-// up to 16 nor a multiple of 16.  The file also holds the merge kernel that
+// does not take: group sizes that are neither a power of two up to 16 nor a
+// multiple of 16, and fp8 caches at head sizes 64 and 256.  The file also holds the merge kernel that
 // both split kernels use (one warp per (sequence, head): every split's (m, l)
 // in one round trip, up to eight partial rows in flight, splits merged in a
 // fixed order) and the elementwise rounding kernel behind attn_round_f32.

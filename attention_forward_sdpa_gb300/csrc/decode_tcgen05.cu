@@ -1,6 +1,7 @@
 // decode_tcgen05.cu -- split-KV decode ("gfx942 unified attention, from the
-// math up", sec. 8) for head size 128 as a persistent, TMA-fed, tcgen05
-// kernel.  Decode is bound by HBM bandwidth (each K/V byte is read once and
+// math up", sec. 8) for head sizes 64, 128 and 256 as a persistent, TMA-fed,
+// tcgen05 kernel (the layout notes below are written for 128; 64 uses one
+// channel half, 256 four halves and two O^T accumulators).  Decode is bound by HBM bandwidth (each K/V byte is read once and
 // used for 2 * G flops), so the design goal is a continuous stream of page
 // loads with as few instructions per byte as possible:
 //
