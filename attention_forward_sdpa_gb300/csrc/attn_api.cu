@@ -55,6 +55,10 @@ constexpr uint64_t kDefaultWaitLimitNs = 4000000000ull;   // 4 s per pipeline wa
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// int32 and fp32 arrays (NULL passes: optional arrays are checked for NULL
+// where they are required)
+bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
 bool valid_scale(float s) { return std::isfinite(s) && s > 0.f; }
 
 constexpr float kLog2e = 1.4426950408889634f;
@@ -412,6 +416,9 @@ attn_status_t prefill_impl(void* out, const void* q, const void* k_cache, const 
     return ATTN_ERR_INVALID_ARG;
   if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache))
     return ATTN_ERR_INVALID_ARG;
+  if (!aligned4(block_table) || !aligned4(query_start_loc) || !aligned4(seq_lens) ||
+      !aligned4(lse_out) || !aligned4(status_dev))
+    return ATTN_ERR_INVALID_ARG;
   const int64_t pages_needed = ((int64_t)max_seqlen_k + block_size - 1) / block_size;
   if (block_table_stride < 1 || block_table_stride < pages_needed) return ATTN_ERR_INVALID_ARG;
   const int group = num_q_heads / num_kv_heads;
@@ -584,6 +591,7 @@ attn_status_t attn_fwd_dense_ex(void* out, const void* q, const void* k, const v
   if (batch == 0 || seqlen_q == 0) return ATTN_OK;  // nothing to compute
   if (!out || !q || !k || !v) return ATTN_ERR_INVALID_ARG;
   if (!aligned16(out) || !aligned16(q) || !aligned16(k) || !aligned16(v)) return ATTN_ERR_INVALID_ARG;
+  if (!aligned4(lse_out) || !aligned4(status_dev)) return ATTN_ERR_INVALID_ARG;
   const int64_t out_elem = rounding == ATTN_OUT_F32 ? 4 : 2;
   const int64_t kv_elem = feat.kv_fp8 ? 1 : 2;     // fp8: one byte per element
   for (int i = 0; i < 3; ++i) {
@@ -743,6 +751,8 @@ attn_status_t attn_fwd_decode_ex(void* out, const void* q, const void* k_cache,
   if (!out || !q || !k_cache || !v_cache || !block_table || !seq_lens) return ATTN_ERR_INVALID_ARG;
   if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache))
     return ATTN_ERR_INVALID_ARG;
+  if (!aligned4(block_table) || !aligned4(seq_lens) || !aligned4(lse_out) || !aligned4(status_dev))
+    return ATTN_ERR_INVALID_ARG;
   const int64_t pages_needed = ((int64_t)max_seqlen_k + block_size - 1) / block_size;
   if (block_table_stride < 1 || block_table_stride < pages_needed) return ATTN_ERR_INVALID_ARG;
   const size_t need = attn_decode_workspace_size(num_seqs, num_q_heads, head_size, num_splits);
@@ -808,6 +818,7 @@ attn_status_t attn_round_f32(void* out, const float* in, int64_t n, attn_dtype_t
   if (rounding < ATTN_RTNE || rounding > ATTN_RTZ) return ATTN_ERR_INVALID_ARG;
   if (n == 0) return ATTN_OK;
   if (!out || !in) return ATTN_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(out) & 1u) || !aligned4(in)) return ATTN_ERR_INVALID_ARG;
   attn_status_t st = check_device();
   if (st != ATTN_OK) return st;
   cudaError_t e = attn::launch_round(out, in, n, dtype == ATTN_BF16, (int)rounding,

@@ -84,6 +84,11 @@ extern "C" attn_status_t attn_fwd_decode_noalloc(
   const uintptr_t mis = reinterpret_cast<uintptr_t>(out) | reinterpret_cast<uintptr_t>(q) |
                         reinterpret_cast<uintptr_t>(k_cache) | reinterpret_cast<uintptr_t>(v_cache);
   if (mis & 15u) return ATTN_ERR_INVALID_ARG;
+  const uintptr_t mis4 = reinterpret_cast<uintptr_t>(block_table) |
+                         reinterpret_cast<uintptr_t>(seq_lens) |
+                         reinterpret_cast<uintptr_t>(lse_out) |
+                         reinterpret_cast<uintptr_t>(status_dev);
+  if (mis4 & 3u) return ATTN_ERR_INVALID_ARG;
   const int64_t pages_needed = ((int64_t)max_seqlen_k + block_size - 1) / block_size;
   if (block_table_stride < 1 || block_table_stride < pages_needed) return ATTN_ERR_INVALID_ARG;
   if (num_seqs > 65535 || num_q_heads > 65535) return ATTN_ERR_UNSUPPORTED;

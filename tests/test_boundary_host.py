@@ -100,6 +100,11 @@ def prefill_args(**over):
     (dict(bt_stride=3), 1),
     (dict(num_seqs=-1), 1),
     (dict(q=ctypes.c_void_p(0x10008)), 1),
+    (dict(bt=ctypes.c_void_p(0x10002)), 1),      # int32 / fp32 arrays: 4-byte aligned
+    (dict(qsl=ctypes.c_void_p(0x10001)), 1),
+    (dict(sl=ctypes.c_void_p(0x10003)), 1),
+    (dict(lse=ctypes.c_void_p(0x10002)), 1),
+    (dict(status=ctypes.c_void_p(0x10001)), 1),
 ])
 def test_prefill_rejects_bad_arguments(lib, over, code):
     assert lib.attn_fwd_prefill(*prefill_args(**over)) == code
@@ -134,9 +139,30 @@ def decode_args(**over):
     (dict(ws_bytes=100), 4),
     (dict(ws=ctypes.c_void_p(0x10004)), 4),
     (dict(rounding=4), 1),
+    (dict(bt=ctypes.c_void_p(0x10002)), 1),
+    (dict(sl=ctypes.c_void_p(0x10001)), 1),
+    (dict(lse=ctypes.c_void_p(0x10003)), 1),
+    (dict(status=ctypes.c_void_p(0x10002)), 1),
 ])
 def test_decode_rejects_bad_arguments(lib, over, code):
     assert lib.attn_fwd_decode(*decode_args(**over)) == code
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(q=None), 1),
+    (dict(q=ctypes.c_void_p(0x10008)), 1),
+    (dict(bt=ctypes.c_void_p(0x10002)), 1),
+    (dict(sl=ctypes.c_void_p(0x10001)), 1),
+    (dict(lse=ctypes.c_void_p(0x10003)), 1),
+    (dict(status=ctypes.c_void_p(0x10002)), 1),
+    (dict(d=80), 2),
+    (dict(splits=65), 1),
+    (dict(num_seqs=0), 0),
+])
+def test_noalloc_decode_rejects_bad_arguments(lib, over, code):
+    a = decode_args(**over)
+    del a[19:21]                                  # no workspace arguments
+    assert lib.attn_fwd_decode_noalloc(*a) == code
 
 
 S3 = (ctypes.c_int64 * 3)
@@ -169,6 +195,8 @@ def dense_args(**over):
     (dict(scale=-1.0), 1),
     (dict(b=-1), 1),
     (dict(q=ctypes.c_void_p(0x10008)), 1),
+    (dict(lse=ctypes.c_void_p(0x10002)), 1),
+    (dict(status=ctypes.c_void_p(0x10001)), 1),
 ])
 def test_dense_rejects_bad_arguments(lib, over, code):
     assert lib.attn_fwd_dense(*dense_args(**over)) == code
@@ -234,6 +262,8 @@ def test_round_rejects_bad_arguments(lib):
     assert lib.attn_round_f32(FAKE, FAKE, -1, 1, 0, None) == 1
     assert lib.attn_round_f32(FAKE, FAKE, 10, 1, 3, None) == 1
     assert lib.attn_round_f32(None, FAKE, 10, 1, 0, None) == 1
+    assert lib.attn_round_f32(ctypes.c_void_p(0x10001), FAKE, 10, 1, 0, None) == 1   # 2-byte out
+    assert lib.attn_round_f32(FAKE, ctypes.c_void_p(0x10002), 10, 1, 0, None) == 1   # 4-byte in
     assert lib.attn_round_f32(FAKE, FAKE, 0, 1, 0, None) == 0
 
 
