@@ -147,6 +147,28 @@ def _dev(t: torch.Tensor, name: str, dtype=None):
     return t
 
 
+def _same_device(dev, **tensors):
+    """Every given tensor on `dev` (the query's device): the library launches
+    on the current device, which the calls below set to `dev`."""
+    for name, t in tensors.items():
+        if t is not None and t.device != dev:
+            raise ValueError(f"{name} is on {t.device}, q on {dev}")
+
+
+def _check_out_arrays(lse, lse_shape, status):
+    """lse (when given) holds exactly one fp32 per (row, head); status (when
+    given) at least one int32 word."""
+    if lse is not None and tuple(lse.shape) != tuple(lse_shape):
+        raise ValueError(f"lse must have shape {tuple(lse_shape)}, got {tuple(lse.shape)}")
+    if status is not None and status.numel() < 1:
+        raise ValueError("status must hold at least one int32 word")
+
+
+def _dims(t, n, name):
+    if t.dim() != n:
+        raise ValueError(f"{name} must be {n}-D, got {t.dim()}-D")
+
+
 def _stream_handle(stream) -> ctypes.c_void_p:
     if stream is None:
         stream = torch.cuda.current_stream()
@@ -262,23 +284,32 @@ def attn_fwd_prefill(out, q, k_cache, v_cache, block_table, query_start_loc, seq
         _dev(lse, "lse", torch.float32)
     if status is not None:
         _dev(status, "status", torch.int32)
+    _dims(q, 3, "q")
+    _dims(k_cache, 4, "k_cache")
     total_q, hq, d = q.shape
     nb, bs, hkv, d2 = k_cache.shape
     if d2 != d or tuple(v_cache.shape) != tuple(k_cache.shape) or tuple(out.shape) != tuple(q.shape):
         raise ValueError("inconsistent q / k_cache / v_cache / out shapes")
+    _dims(seq_lens, 1, "seq_lens")
     num_seqs = seq_lens.shape[0]
-    if query_start_loc.shape[0] != num_seqs + 1 or block_table.dim() != 2 or \
-            block_table.shape[0] != num_seqs:
+    if query_start_loc.dim() != 1 or query_start_loc.shape[0] != num_seqs + 1 or \
+            block_table.dim() != 2 or block_table.shape[0] != num_seqs:
         raise ValueError("inconsistent query_start_loc / block_table / seq_lens shapes")
-    args = (_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table),
-            block_table.shape[1], _ptr(query_start_loc), _ptr(seq_lens), num_seqs,
-            int(max_seqlen_q), int(max_seqlen_k), total_q, hq, hkv, d, bs, nb, float(scale),
-            int(bool(causal)), dt, int(rounding), _ptr(lse), _ptr(status), _stream_handle(stream))
-    feat = _features(hq, window, softcap, alibi_slopes, sinks, kv_scales, fp8_workspace)
-    if feat is None:
-        _check(lib.attn_fwd_prefill(*args), "attn_fwd_prefill")
-    else:
-        _check(lib.attn_fwd_prefill_ex(*args, ctypes.byref(feat)), "attn_fwd_prefill_ex")
+    _check_out_arrays(lse, (total_q, hq), status)
+    _same_device(q.device, out=out, k_cache=k_cache, v_cache=v_cache, block_table=block_table,
+                 query_start_loc=query_start_loc, seq_lens=seq_lens, lse=lse, status=status,
+                 alibi_slopes=alibi_slopes, sinks=sinks, fp8_workspace=fp8_workspace)
+    with torch.cuda.device(q.device):
+        args = (_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table),
+                block_table.shape[1], _ptr(query_start_loc), _ptr(seq_lens), num_seqs,
+                int(max_seqlen_q), int(max_seqlen_k), total_q, hq, hkv, d, bs, nb, float(scale),
+                int(bool(causal)), dt, int(rounding), _ptr(lse), _ptr(status),
+                _stream_handle(stream))
+        feat = _features(hq, window, softcap, alibi_slopes, sinks, kv_scales, fp8_workspace)
+        if feat is None:
+            _check(lib.attn_fwd_prefill(*args), "attn_fwd_prefill")
+        else:
+            _check(lib.attn_fwd_prefill_ex(*args, ctypes.byref(feat)), "attn_fwd_prefill_ex")
 
 
 def _strides3(t, name):
@@ -320,14 +351,18 @@ def attn_fwd_dense(out, q, k, v, *, scale: float, causal: bool, rounding: int = 
     b2, sk, hkv, d2 = k.shape
     if b2 != b or d2 != d or tuple(v.shape) != tuple(k.shape) or tuple(out.shape) != tuple(q.shape):
         raise ValueError("inconsistent q / k / v / out shapes")
-    args = (_ptr(out), _ptr(q), _ptr(k), _ptr(v), qs, ks, vs, os_, b, sq, sk, hq, hkv, d,
-            float(scale), int(bool(causal)), dt, int(rounding), _ptr(lse), _ptr(status),
-            _stream_handle(stream))
-    feat = _features(hq, window, softcap, alibi_slopes, sinks, kv_scales, fp8_workspace)
-    if feat is None:
-        _check(lib.attn_fwd_dense(*args), "attn_fwd_dense")
-    else:
-        _check(lib.attn_fwd_dense_ex(*args, ctypes.byref(feat)), "attn_fwd_dense_ex")
+    _check_out_arrays(lse, (b, hq, sq), status)
+    _same_device(q.device, out=out, k=k, v=v, lse=lse, status=status, alibi_slopes=alibi_slopes,
+                 sinks=sinks, fp8_workspace=fp8_workspace)
+    with torch.cuda.device(q.device):
+        args = (_ptr(out), _ptr(q), _ptr(k), _ptr(v), qs, ks, vs, os_, b, sq, sk, hq, hkv, d,
+                float(scale), int(bool(causal)), dt, int(rounding), _ptr(lse), _ptr(status),
+                _stream_handle(stream))
+        feat = _features(hq, window, softcap, alibi_slopes, sinks, kv_scales, fp8_workspace)
+        if feat is None:
+            _check(lib.attn_fwd_dense(*args), "attn_fwd_dense")
+        else:
+            _check(lib.attn_fwd_dense_ex(*args, ctypes.byref(feat)), "attn_fwd_dense_ex")
 
 
 def attn_fwd_decode(out, q, k_cache, v_cache, block_table, seq_lens, *, max_seqlen_k: int,
@@ -352,21 +387,29 @@ def attn_fwd_decode(out, q, k_cache, v_cache, block_table, seq_lens, *, max_seql
     if workspace is not None:
         _dev(workspace, "workspace")
         ws_bytes = workspace.numel() * workspace.element_size()
+    _dims(q, 3, "q")
+    _dims(k_cache, 4, "k_cache")
     num_seqs, hq, d = q.shape
     nb, bs, hkv, d2 = k_cache.shape
     if d2 != d or tuple(v_cache.shape) != tuple(k_cache.shape) or tuple(out.shape) != tuple(q.shape):
         raise ValueError("inconsistent q / k_cache / v_cache / out shapes")
-    if seq_lens.shape[0] != num_seqs or block_table.dim() != 2 or block_table.shape[0] != num_seqs:
+    if seq_lens.dim() != 1 or seq_lens.shape[0] != num_seqs or block_table.dim() != 2 or \
+            block_table.shape[0] != num_seqs:
         raise ValueError("inconsistent block_table / seq_lens shapes")
-    args = (_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table),
-            block_table.shape[1], _ptr(seq_lens), num_seqs, int(max_seqlen_k), hq, hkv, d, bs, nb,
-            float(scale), int(num_splits), dt, int(rounding), _ptr(lse), _ptr(workspace),
-            ws_bytes, _ptr(status), _stream_handle(stream))
-    feat = _features(hq, window, softcap, alibi_slopes, sinks, kv_scales)
-    if feat is None:
-        _check(lib.attn_fwd_decode(*args), "attn_fwd_decode")
-    else:
-        _check(lib.attn_fwd_decode_ex(*args, ctypes.byref(feat)), "attn_fwd_decode_ex")
+    _check_out_arrays(lse, (num_seqs, hq), status)
+    _same_device(q.device, out=out, k_cache=k_cache, v_cache=v_cache, block_table=block_table,
+                 seq_lens=seq_lens, lse=lse, status=status, workspace=workspace,
+                 alibi_slopes=alibi_slopes, sinks=sinks)
+    with torch.cuda.device(q.device):
+        args = (_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table),
+                block_table.shape[1], _ptr(seq_lens), num_seqs, int(max_seqlen_k), hq, hkv, d, bs,
+                nb, float(scale), int(num_splits), dt, int(rounding), _ptr(lse), _ptr(workspace),
+                ws_bytes, _ptr(status), _stream_handle(stream))
+        feat = _features(hq, window, softcap, alibi_slopes, sinks, kv_scales)
+        if feat is None:
+            _check(lib.attn_fwd_decode(*args), "attn_fwd_decode")
+        else:
+            _check(lib.attn_fwd_decode_ex(*args, ctypes.byref(feat)), "attn_fwd_decode_ex")
 
 
 def attn_fwd_decode_noalloc(out, q, k_cache, v_cache, block_table, seq_lens, *,
@@ -388,17 +431,24 @@ def attn_fwd_decode_noalloc(out, q, k_cache, v_cache, block_table, seq_lens, *,
         _dev(lse, "lse", torch.float32)
     if status is not None:
         _dev(status, "status", torch.int32)
+    _dims(q, 3, "q")
+    _dims(k_cache, 4, "k_cache")
     num_seqs, hq, d = q.shape
     nb, bs, hkv, d2 = k_cache.shape
     if d2 != d or tuple(v_cache.shape) != tuple(k_cache.shape) or tuple(out.shape) != tuple(q.shape):
         raise ValueError("inconsistent q / k_cache / v_cache / out shapes")
-    if seq_lens.shape[0] != num_seqs or block_table.dim() != 2 or block_table.shape[0] != num_seqs:
+    if seq_lens.dim() != 1 or seq_lens.shape[0] != num_seqs or block_table.dim() != 2 or \
+            block_table.shape[0] != num_seqs:
         raise ValueError("inconsistent block_table / seq_lens shapes")
-    rc = lib.attn_fwd_decode_noalloc(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache),
-                                     _ptr(block_table), block_table.shape[1], _ptr(seq_lens),
-                                     num_seqs, int(max_seqlen_k), hq, hkv, d, bs, nb, float(scale),
-                                     int(num_splits), dt, int(rounding), _ptr(lse), _ptr(status),
-                                     _stream_handle(stream))
+    _check_out_arrays(lse, (num_seqs, hq), status)
+    _same_device(q.device, out=out, k_cache=k_cache, v_cache=v_cache, block_table=block_table,
+                 seq_lens=seq_lens, lse=lse, status=status)
+    with torch.cuda.device(q.device):
+        rc = lib.attn_fwd_decode_noalloc(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache),
+                                         _ptr(block_table), block_table.shape[1], _ptr(seq_lens),
+                                         num_seqs, int(max_seqlen_k), hq, hkv, d, bs, nb,
+                                         float(scale), int(num_splits), dt, int(rounding),
+                                         _ptr(lse), _ptr(status), _stream_handle(stream))
     _check(rc, "attn_fwd_decode_noalloc")
 
 
@@ -410,8 +460,10 @@ def attn_round_f32(out, x, *, dtype: torch.dtype, rounding: int, stream=None) ->
     _dev(out, "out")
     if out.element_size() != 2 or out.numel() != x.numel():
         raise ValueError("out must be a 16-bit tensor with as many elements as x")
-    _check(lib.attn_round_f32(_ptr(out), _ptr(x), x.numel(), _dtype_code(dtype), int(rounding),
-                              _stream_handle(stream)), "attn_round_f32")
+    _same_device(x.device, out=out)
+    with torch.cuda.device(x.device):
+        _check(lib.attn_round_f32(_ptr(out), _ptr(x), x.numel(), _dtype_code(dtype),
+                                  int(rounding), _stream_handle(stream)), "attn_round_f32")
 
 
 # ----------------------------------------------------------------------------
