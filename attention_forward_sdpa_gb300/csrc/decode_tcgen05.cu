@@ -1,9 +1,10 @@
 // decode_tcgen05.cu -- split-KV decode ("gfx942 unified attention, from the
 // math up", sec. 8) for head sizes 64, 128 and 256 as a persistent, TMA-fed,
 // tcgen05 kernel (the layout notes below are written for 128; 64 uses one
-// channel half, 256 four halves and two O^T accumulators).  Decode is bound by HBM bandwidth (each K/V byte is read once and
-// used for 2 * G flops), so the design goal is a continuous stream of page
-// loads with as few instructions per byte as possible:
+// channel half, 256 four halves and two O^T accumulators).  Decode is bound
+// by HBM bandwidth (each K/V byte is read once and used for 2 * G flops), so
+// the design goal is a continuous stream of page loads with as few
+// instructions per byte as possible:
 //
 //   * A work item is (sequence, F consecutive KV heads, split) -- F KV heads
 //     and all their query heads (F * G <= 16) at once, so that one TMA box
@@ -16,9 +17,10 @@
 //   * Persistent CTAs (one per SM) claim items from an atomic counter in
 //     longest-sequence-first order (each CTA ranks the sequence lengths it
 //     caches in shared memory), so items balance dynamically.
-//   * Warp 0 streams Q rows and page boxes into a ring of 32 KB tiles (K and
-//     V alternate); its lanes hold the page ids of 64 boxes at a time and
-//     issue the boxes in parallel.
+//   * Warp 0 streams Q rows and page boxes into a 192 KB ring of 128-row
+//     tiles (K and V alternate; six tiles of 32 KB at head size 128, twelve
+//     of 16 KB at 64, three of 64 KB at 256); its lanes hold the page ids of
+//     64 boxes at a time and issue the boxes in parallel.
 //   * Warp 1 issues S^T = K Q^T (M = 128 tile rows, N = 16 query heads, fp32
 //     in TMEM) and O^T += V^T P^T (M = 128 channels, N = 16).  P^T is block
 //     diagonal (a row of KV head h only feeds the columns of h's query
@@ -67,7 +69,7 @@ struct ItemEntry {
 
 constexpr int kStage8Bytes = kRows * 128;      // an fp8 tile: 128 rows x 128 codes (16 KB)
 
-// Shared-memory layout.  With 16-bit caches the ring holds six tiles.  With
+// Shared-memory layout.  With 16-bit caches the ring holds 192 KB of tiles.  With
 // fp8 caches (KV8) TMA lands the codes in four 16 KB staging tiles, four
 // converter warps widen them into a ring of four 16-bit tiles (the layout
 // the MMAs read), and the CTA has 320 threads instead of 192.
@@ -79,7 +81,7 @@ struct Lay {
   static constexpr int kOBlocks = D == 256 ? 2 : 1;      // 128-channel blocks of O^T (TMEM)
   static constexpr int kSeqCache = D == 256 ? 1024 : 2048;   // cached sequence lengths
   static constexpr int kHalves = D / 64;                 // 64-channel halves of a row
-  static constexpr int kTileBytes = kRows * D * 2;       // 32 KB (d = 128), 16 KB (d = 64)
+  static constexpr int kTileBytes = kRows * D * 2;       // 16 / 32 / 64 KB at d = 64 / 128 / 256
   static constexpr int kQBytes = kHalves * 16 * 128;     // channel halves of [16 heads][64]
   static constexpr int kVGroup = kHalves * 2048;         // V: one 16-row group, all halves
   static constexpr int kThreads = KV8 ? 320 : 192;
