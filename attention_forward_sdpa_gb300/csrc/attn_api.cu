@@ -73,7 +73,6 @@ struct Features {
   float k_scale = 1.f, v_scale = 1.f;
   void* workspace = nullptr;
   size_t workspace_bytes = 0;
-  bool any() const { return win_left >= 0 || win_right >= 0 || softcap > 0.f || alibi || sinks; }
 };
 
 attn_status_t read_features(const attn_features_t* f, Features& out) {
