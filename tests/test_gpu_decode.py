@@ -4,7 +4,8 @@ fp64 oracle ("gfx942 unified attention, from the math up", sec. 8).
 Tolerance: 4e-2 (bf16) / 2e-2 (fp16) max |err| vs the oracle, as for prefill.
 Covers the full decode workload (64 sequences, kv lengths uniform in
 [512, 8192], block size 16, GQA 4:1, 8 splits), every heads-per-CTA variant,
-head size 64 and fp16, split counts 1..64, tiny and empty sequences, the
+head size 64 and fp16, split counts 1..64, batches of up to 2300 sequences
+(each way the kernel holds the sequence lengths), tiny and empty sequences, the
 log-sum-exp output, bit identity across runs, and device-side reporting of a
 bad block-table entry.
 """
@@ -47,6 +48,25 @@ def test_head_groups(hq, hkv):
                                      num_q_heads=hq, num_kv_heads=hkv, head_size=128,
                                      block_size=16, causal=False, pool_extra=4)
     check(prob)
+
+
+# The persistent kernel orders work items longest sequence first when the
+# batch is small enough to rank in shared memory, keeps the sequence lengths
+# in shared memory for larger batches, and reads them from global memory
+# beyond that (the thresholds differ by head size); each regime, on both
+# sides of its threshold, must give the same results.
+@pytest.mark.parametrize("d,n,splits", [(128, 128, 8), (128, 129, 8), (128, 700, 3),
+                                        (128, 2048, 8), (128, 2049, 1), (128, 2300, 8),
+                                        (64, 2100, 8), (256, 1024, 8), (256, 1025, 2),
+                                        (256, 1300, 8)])
+def test_many_sequences(d, n, splits):
+    rng = np.random.default_rng(n + d)
+    kv_lens = [int(x) for x in rng.integers(0, 90, size=n)]
+    kv_lens[n // 2] = 700                               # one long sequence in the middle
+    prob = attn_inputs.paged_problem(seed=35 + n, q_lens=[1] * n, kv_lens=kv_lens, num_q_heads=8,
+                                     num_kv_heads=2, head_size=d, block_size=16, causal=False,
+                                     pool_extra=2)
+    check(prob, splits=splits)
 
 
 @pytest.mark.parametrize("splits", [1, 2, 3, 8, 64])
