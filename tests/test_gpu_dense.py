@@ -64,6 +64,7 @@ CASES = {
     "gqa2_bf16_d128_noncausal_short_keys": (3, 129, 17, 4, 2, 128, torch.bfloat16, False),
     "mha_bf16_d128_causal_square": (2, 384, 384, 2, 2, 128, torch.bfloat16, True),
     "gqa8_fp16_d128_causal": (1, 257, 512, 16, 2, 128, torch.float16, True),
+    "gqa2_bf16_d128_causal_many_batches": (600, 24, 40, 4, 2, 128, torch.bfloat16, True),
 }
 
 

@@ -7,10 +7,10 @@ compare the full tensor for the 128, 2048 and chunked workloads and a row
 sample for the 8192 and dense ones (every sequence and head: first, second,
 last two rows and 256 random rows -- rows are independent, so each sampled
 row is exact).
-Also: run-to-run bit identity, invariance to paging (block size and
-permutation), GQA vs materialised MHA, rows without visible keys, and the
-epilogue rounding against the oracle's rounding of the kernel's own fp32
-result.
+Also: a batch of 300 short sequences, run-to-run bit identity, invariance to
+paging (block size and permutation), GQA vs materialised MHA, rows without
+visible keys, and the epilogue rounding against the oracle's rounding of the
+kernel's own fp32 result.
 """
 import numpy as np
 import pytest
@@ -64,6 +64,24 @@ SMALL = {
 @pytest.mark.parametrize("name", sorted(SMALL))
 def test_small_cases_match_oracle(name):
     prob = attn_inputs.paged_problem(seed=21, pool_extra=5, **SMALL[name])
+    check_full(prob)
+
+
+@pytest.mark.parametrize("d,causal,bs", [(128, True, 64), (128, False, 16), (64, True, 128),
+                                         (256, True, 32)])
+def test_many_sequences(d, causal, bs):
+    """A batch of 300 short sequences (some with no query rows, some with no
+    keys): one grid row per sequence, most CTAs of the longest row block exit
+    at once."""
+    rng = np.random.default_rng(d + bs)
+    q_lens = [int(x) for x in rng.integers(0, 140, size=300)]
+    q_lens[7] = 0
+    kv_lens = [q + int(rng.integers(0, 40)) for q in q_lens]
+    kv_lens[11] = 0
+    q_lens[11] = 0 if causal else q_lens[11]
+    prob = attn_inputs.paged_problem(seed=40 + d, q_lens=q_lens, kv_lens=kv_lens, num_q_heads=4,
+                                     num_kv_heads=2, head_size=d, block_size=bs, causal=causal,
+                                     pool_extra=3)
     check_full(prob)
 
 
