@@ -42,7 +42,7 @@ def test_workload_decode_other_head_sizes(name):
 
 
 @pytest.mark.parametrize("hq,hkv", [(8, 8), (8, 4), (8, 2), (16, 2), (24, 2), (12, 4), (16, 1),
-                                     (32, 1), (40, 2)])
+                                     (32, 1), (40, 2), (48, 1), (64, 4), (2, 1)])
 def test_head_groups(hq, hkv):
     prob = attn_inputs.paged_problem(seed=31, q_lens=[1] * 5, kv_lens=[1, 16, 17, 300, 2049],
                                      num_q_heads=hq, num_kv_heads=hkv, head_size=128,
