@@ -27,6 +27,7 @@ bytes (the allocating ``prefill`` creates it).
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 import threading
@@ -150,9 +151,17 @@ def _dev(t: torch.Tensor, name: str, dtype=None):
 def _same_device(dev, **tensors):
     """Every given tensor on `dev` (the query's device): the library launches
     on the current device, which the calls below set to `dev`."""
+    idx = dev.index
     for name, t in tensors.items():
-        if t is not None and t.device != dev:
+        if t is not None and t.get_device() != idx:
             raise ValueError(f"{name} is on {t.device}, q on {dev}")
+
+
+def _on(dev):
+    """Makes `dev` the current device for the call (no switch when it is)."""
+    if dev.index == torch.cuda.current_device():
+        return contextlib.nullcontext()
+    return torch.cuda.device(dev)
 
 
 def _check_out_arrays(lse, lse_shape, status):
@@ -170,9 +179,15 @@ def _dims(t, n, name):
 
 
 def _stream_handle(stream) -> ctypes.c_void_p:
+    """The cudaStream_t of `stream` (None: the current stream of the current
+    device, which the calls set to the query's device).  A torch stream must
+    belong to that device; a raw handle is passed through as given."""
     if stream is None:
         stream = torch.cuda.current_stream()
     if isinstance(stream, torch.cuda.Stream):
+        if stream.device.index != torch.cuda.current_device():
+            raise ValueError(f"stream is on {stream.device}, the call on "
+                             f"cuda:{torch.cuda.current_device()}")
         return ctypes.c_void_p(stream.cuda_stream)
     return ctypes.c_void_p(int(stream))
 
@@ -299,7 +314,7 @@ def attn_fwd_prefill(out, q, k_cache, v_cache, block_table, query_start_loc, seq
     _same_device(q.device, out=out, k_cache=k_cache, v_cache=v_cache, block_table=block_table,
                  query_start_loc=query_start_loc, seq_lens=seq_lens, lse=lse, status=status,
                  alibi_slopes=alibi_slopes, sinks=sinks, fp8_workspace=fp8_workspace)
-    with torch.cuda.device(q.device):
+    with _on(q.device):
         args = (_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table),
                 block_table.shape[1], _ptr(query_start_loc), _ptr(seq_lens), num_seqs,
                 int(max_seqlen_q), int(max_seqlen_k), total_q, hq, hkv, d, bs, nb, float(scale),
@@ -354,7 +369,7 @@ def attn_fwd_dense(out, q, k, v, *, scale: float, causal: bool, rounding: int = 
     _check_out_arrays(lse, (b, hq, sq), status)
     _same_device(q.device, out=out, k=k, v=v, lse=lse, status=status, alibi_slopes=alibi_slopes,
                  sinks=sinks, fp8_workspace=fp8_workspace)
-    with torch.cuda.device(q.device):
+    with _on(q.device):
         args = (_ptr(out), _ptr(q), _ptr(k), _ptr(v), qs, ks, vs, os_, b, sq, sk, hq, hkv, d,
                 float(scale), int(bool(causal)), dt, int(rounding), _ptr(lse), _ptr(status),
                 _stream_handle(stream))
@@ -400,7 +415,7 @@ def attn_fwd_decode(out, q, k_cache, v_cache, block_table, seq_lens, *, max_seql
     _same_device(q.device, out=out, k_cache=k_cache, v_cache=v_cache, block_table=block_table,
                  seq_lens=seq_lens, lse=lse, status=status, workspace=workspace,
                  alibi_slopes=alibi_slopes, sinks=sinks)
-    with torch.cuda.device(q.device):
+    with _on(q.device):
         args = (_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table),
                 block_table.shape[1], _ptr(seq_lens), num_seqs, int(max_seqlen_k), hq, hkv, d, bs,
                 nb, float(scale), int(num_splits), dt, int(rounding), _ptr(lse), _ptr(workspace),
@@ -443,7 +458,7 @@ def attn_fwd_decode_noalloc(out, q, k_cache, v_cache, block_table, seq_lens, *,
     _check_out_arrays(lse, (num_seqs, hq), status)
     _same_device(q.device, out=out, k_cache=k_cache, v_cache=v_cache, block_table=block_table,
                  seq_lens=seq_lens, lse=lse, status=status)
-    with torch.cuda.device(q.device):
+    with _on(q.device):
         rc = lib.attn_fwd_decode_noalloc(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache),
                                          _ptr(block_table), block_table.shape[1], _ptr(seq_lens),
                                          num_seqs, int(max_seqlen_k), hq, hkv, d, bs, nb,
@@ -461,7 +476,7 @@ def attn_round_f32(out, x, *, dtype: torch.dtype, rounding: int, stream=None) ->
     if out.element_size() != 2 or out.numel() != x.numel():
         raise ValueError("out must be a 16-bit tensor with as many elements as x")
     _same_device(x.device, out=out)
-    with torch.cuda.device(x.device):
+    with _on(x.device):
         _check(lib.attn_round_f32(_ptr(out), _ptr(x), x.numel(), _dtype_code(dtype),
                                   int(rounding), _stream_handle(stream)), "attn_round_f32")
 

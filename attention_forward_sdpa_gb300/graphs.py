@@ -58,7 +58,8 @@ class GraphCache:
 
     def run(self, key, tensors, fn) -> None:
         """fn(stream) enqueues the call on `stream`; it is captured on first use
-        of `key` and replayed on the current stream from then on."""
+        of `key` and replayed on the current stream from then on.  The
+        caller makes the tensors' device current."""
         cur = torch.cuda.current_stream()
         if torch.cuda.is_current_stream_capturing():
             fn(cur)                      # the caller's own capture records it
@@ -103,8 +104,7 @@ def decode(out, q, k_cache, v_cache, block_table, seq_lens, *, max_seqlen_k: int
     if not should_graph(1, has_features(**features)):
         attn_fwd_decode(out, q, k_cache, v_cache, block_table, seq_lens,
                         max_seqlen_k=max_seqlen_k, scale=scale, num_splits=num_splits,
-                        workspace=workspace, rounding=rounding, lse=lse,
-                        stream=torch.cuda.current_stream(), **features)
+                        workspace=workspace, rounding=rounding, lse=lse, **features)
         return False
     cache = _default if cache is None else cache
     tensors = (out, q, k_cache, v_cache, block_table, seq_lens, workspace, lse)
@@ -116,7 +116,8 @@ def decode(out, q, k_cache, v_cache, block_table, seq_lens, *, max_seqlen_k: int
                         max_seqlen_k=max_seqlen_k, scale=scale, num_splits=num_splits,
                         workspace=workspace, rounding=rounding, lse=lse, stream=stream)
 
-    cache.run(key, tensors, fn)
+    with torch.cuda.device(q.device):
+        cache.run(key, tensors, fn)
     return True
 
 
@@ -131,13 +132,14 @@ def prefill(out, q, k_cache, v_cache, block_table, query_start_loc, seq_lens, *,
                          causal=causal, rounding=rounding, lse=lse, stream=stream, **features)
 
     if not should_graph(max_seqlen_q, has_features(**features)):
-        fn(torch.cuda.current_stream())
+        fn(None)                         # the query device's current stream
         return False
     cache = _default if cache is None else cache
     tensors = (out, q, k_cache, v_cache, block_table, query_start_loc, seq_lens, lse)
     key = _key("prefill", tensors, (int(max_seqlen_q), int(max_seqlen_k), float(scale),
                                     bool(causal), int(rounding)))
-    cache.run(key, tensors, fn)
+    with torch.cuda.device(q.device):
+        cache.run(key, tensors, fn)
     return True
 
 
