@@ -36,9 +36,9 @@ def _worker(rank, world, port, results):
 def test_two_gloo_ranks_reduce_like_the_bench():
     world = 2
     port = _free_port()
-    with mp.Manager() as m:
+    ctx = mp.get_context("spawn")     # no fork of a process that already runs threads
+    with ctx.Manager() as m:
         results = m.dict()
-        ctx = mp.get_context("spawn")
         procs = [ctx.Process(target=_worker, args=(r, world, port, results)) for r in range(world)]
         for p in procs:
             p.start()
