@@ -378,7 +378,7 @@ static void one_row(const problem_t *p, int64_t t, int32_t h, double *o,
         int64_t per = (limit + P - 1) / P;
         per = (per + 15) / 16 * 16;
         double part_lse[256];
-        double *part_o = (double *)calloc((size_t)P * d, sizeof(double));
+        double *part_o = (double *)calloc((size_t)P * (size_t)d, sizeof(double));
         for (int64_t q = 0; q < P; ++q) {
             int64_t j0 = q * per, j1 = (q + 1) * per < limit ? (q + 1) * per : limit;
             if (j0 >= j1) { part_lse[q] = -INFINITY; continue; }
