@@ -28,7 +28,8 @@
  *     entry point (16 bytes or more); int32 and fp32 arrays (block tables,
  *     query_start_loc, seq_lens, lse_out, status_dev, the fp32 input of
  *     attn_round_f32) on 4 bytes; the output of attn_round_f32 on 2.  A
- *     misaligned pointer is ATTN_ERR_INVALID_ARG.
+ *     misaligned pointer is ATTN_ERR_INVALID_ARG (a misaligned workspace
+ *     ATTN_ERR_WORKSPACE).
  *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL is the legacy
  *     default stream).  Inputs must stay valid until the work completes.
  *   - Argument errors are detected on the host and returned before anything
