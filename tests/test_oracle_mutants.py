@@ -14,6 +14,7 @@ import pytest
 import torch
 
 from oracle import oracle
+from tests import test_oracle_feature_pins as feature_pins
 from tests import test_oracle_fp8_pins as fp8_pins
 from tests import test_oracle_pins as pins
 
@@ -40,6 +41,22 @@ def _widen_pins():
     pins.test_widen_all_patterns(oracle.BF16, torch.bfloat16)
     pins.test_widen_all_patterns(oracle.F16, torch.float16)
     fp8_pins.test_widen8_matches_torch_on_all_patterns()
+
+
+def _recurrence_pins():
+    for tile in (3, 16):
+        pins.test_streaming_recurrence_equals_definition(tile)
+    for parts in (2, 8, 13):
+        pins.test_split_combine_equals_definition(parts)
+
+
+def _feature_pins():
+    for left, right in ((3, -1), (0, 2), (2, 5)):
+        feature_pins.test_window_matches_torch_band_mask(left, right)
+    feature_pins.test_saturated_scores_take_plus_minus_cap()
+    feature_pins.test_alibi_geometric_weights_closed_form()
+    feature_pins.test_sink_with_zero_query_closed_form()
+    feature_pins.test_row_without_keys_reports_the_sink()
 
 
 def _fp8_pins():
@@ -69,6 +86,31 @@ MUTANTS = {
                               "if (lse) *lse = m + log2(den);", _sdpa_pins),
     "running max left out of the log-sum-exp": ("if (lse) *lse = m + log(den);",
                                                 "if (lse) *lse = log(den);", _sdpa_pins),
+    # the streaming recurrence and the split combine
+    "streaming: accumulator not rescaled": ("for (int32_t c = 0; c < d; ++c) o[c] *= alpha;",
+                                            "for (int32_t c = 0; c < d; ++c) o[c] *= 1.0;",
+                                            _recurrence_pins),
+    "streaming: denominator not rescaled": ("l = alpha * l + tsum;", "l = l + tsum;",
+                                            _recurrence_pins),
+    "split: parts left unnormalised": ("for (int32_t c = 0; c < d; ++c) po[c] /= den;",
+                                       "for (int32_t c = 0; c < d; ++c) po[c] /= 1.0;",
+                                       _recurrence_pins),
+    "split: combined LSE without the reference max": ("if (lse) *lse = L + log(wsum);",
+                                                      "if (lse) *lse = log(wsum);",
+                                                      _recurrence_pins),
+    # feature flags
+    "window: left bound taken from the right width": (
+        "if (p->win_left >= 0 && diag - p->win_left > lo) lo = diag - p->win_left;",
+        "if (p->win_left >= 0 && diag - p->win_right > lo) lo = diag - p->win_right;",
+        _feature_pins),
+    "softcap: outer factor dropped": (
+        "if (p->softcap > 0.0) x = p->softcap * tanh(x / p->softcap);",
+        "if (p->softcap > 0.0) x = tanh(x / p->softcap);", _feature_pins),
+    "ALiBi bias added instead of subtracted": (
+        "if (p->alibi) x -= p->alibi[h] * fabs((double)(diag - j));",
+        "if (p->alibi) x += p->alibi[h] * fabs((double)(diag - j));", _feature_pins),
+    "sink left out of the denominator": ("double den = p->sinks ? exp(sink - m) : 0.0;",
+                                         "double den = 0.0;", _feature_pins),
     # formats
     "fp16 exponent bias off by one": ("v = ldexp((double)(1024 + f), e - 15 - 10);",
                                       "v = ldexp((double)(1024 + f), e - 16 - 10);",
@@ -78,9 +120,9 @@ MUTANTS = {
     "E4M3 subnormal exponent": ("mag = ldexp((double)f / 8.0, -6);",
                                 "mag = ldexp((double)f / 8.0, -7);", _widen_pins),
     "E4M3 sign ignored": ("return s ? -mag : mag;", "return mag;", _widen_pins),
-    "fp8 K factor ignored": ("acc += qv[c] * cache_at(p, p->k_cache, p->k_scale, b, j, kvh, c);",
-                             "acc += qv[c] * cache_at(p, p->k_cache, 1.0, b, j, kvh, c);",
-                             _fp8_pins),
+    "fp8 K factor ignored": (
+        "acc += qv[c] * cache_at(p, p->k_cache, p->k_scale, b, j, kvh, c);",
+        "acc += qv[c] * cache_at(p, p->k_cache, 1.0, b, j, kvh, c);", _fp8_pins),
     # rounding
     "RTNA rounds ties to even": ("else if (mode == OR_RTNA) up = cmp_half >= 0;",
                                  "else if (mode == OR_RTNA) up = cmp_half > 0;", _rounding_pins),
