@@ -96,3 +96,13 @@ def test_fp8_decode_bytes_count_one_byte_per_cached_element():
     kv_rows = sum(prob.kv_lens)
     d, hkv, hq, b = prob.head_size, prob.num_kv_heads, prob.num_q_heads, prob.num_seqs
     assert bench.decode_bytes(prob) == float(2 * kv_rows * hkv * d + 2 * b * hq * d * 2)
+
+
+def test_code_hash_ignores_comments_and_layout_but_not_code():
+    """The traffic figures in bench.py are tied to the kernel source through
+    this hash: comment and white-space edits keep them, code edits drop them."""
+    a = "int f(int x) {\n  return x + 1;  // one\n}\n/* block\n comment */\n"
+    b = "int f(int x){return x+1;}   // other words\n"
+    c = "int f(int x) { return x + 2; }\n"
+    assert bench.code_hash(a) == bench.code_hash(b)
+    assert bench.code_hash(a) != bench.code_hash(c)
