@@ -57,3 +57,31 @@ def test_nothing_committed_points_into_the_working_folder():
     pattern = re.compile(r"(^|[\s'\"/(])_work/")
     for path in files_under(ROOT, (".py", ".cu", ".cuh", ".h", ".c", ".md", ".txt", ".json")):
         assert not pattern.search(read(path)), os.path.relpath(path, ROOT)
+
+
+CSRC = os.path.join(PKG, "csrc")
+
+
+def test_every_barrier_wait_in_the_kernels_is_bounded():
+    """Every spin on an mbarrier gives up after a time limit (the kernels then
+    record a timeout in the status word and leave), and no device code traps
+    or asserts: a stalled pipeline cannot hang the GPU."""
+    ptx = read(os.path.join(CSRC, "sm103_ptx.cuh"))
+    assert ptx.count("mbarrier.try_wait") == 1          # only inside mbar_test
+    wait = ptx[ptx.index("bool mbar_wait("):]
+    wait = wait[:wait.index("\n}\n")]
+    assert "global_timer_ns() - t0 > limit_ns" in wait and "*abort" in wait
+    for path in files_under(CSRC, (".cu", ".cuh")):
+        text = read(path)
+        if not path.endswith("sm103_ptx.cuh"):
+            assert "mbarrier.try_wait" not in text and "mbarrier.test_wait" not in text, path
+        loops = list(re.finditer(r"while \(!mbar_test\([^)]*\)\) \{", text))
+        if not path.endswith("sm103_ptx.cuh"):
+            # a raw barrier probe appears only as the head of a bounded loop
+            assert len(loops) == text.count("mbar_test("), path
+        for m in loops:
+            body = text[m.end():text.index("}", m.end())]
+            assert "global_timer_ns() - t0 >" in body, (path, text[m.start():m.end()])
+        code = re.sub(r"//[^\n]*|/\*.*?\*/", "", text, flags=re.S)
+        assert "__trap" not in code and "brkpt" not in code, path
+        assert not re.search(r"(?<!static_)assert\s*\(", code), path
