@@ -453,3 +453,22 @@ def test_nan_stays_nan():
         for mode in (oracle.RTNE, oracle.RTNA, oracle.RTZ):
             r = oracle.widen16(oracle.round_f32(x, dt, mode), dt)
             assert np.all(np.isnan(r))
+
+
+# ----------------------------------------------------------------------------
+# the oracle's own threading
+# ----------------------------------------------------------------------------
+
+@pytest.mark.parametrize("variant,param", [(0, 0), (1, 16), (2, 8)])
+def test_thread_count_does_not_change_results(variant, param):
+    """Rows are independent and each is computed by one thread in a fixed
+    order, so the job split across threads must not change a single bit;
+    every row must be written (no row left at its initial value)."""
+    p = attn_inputs.paged_problem(seed=18, q_lens=[37, 1, 90], kv_lens=[50, 300, 90],
+                                  num_q_heads=6, num_kv_heads=3, head_size=16, block_size=16,
+                                  causal=True)
+    ref_out, ref_lse = run(p, variant=variant, param=param, threads=1)
+    assert np.isfinite(ref_out).all() and np.isfinite(ref_lse).all()
+    for threads in (2, 3, 7, 64):
+        out, lse = run(p, variant=variant, param=param, threads=threads)
+        assert np.array_equal(out, ref_out) and np.array_equal(lse, ref_lse), threads
