@@ -1,7 +1,7 @@
 """Host-side checks of the C ABI (no GPU needed, nothing is launched).
 
   - the shared library builds, loads and exports every function that
-    include/attn_fwd.h declares;
+    include/attn_fwd.h declares, and the header serves a plain C99 program;
   - argument errors are returned before any CUDA call (so they work on a
     machine without a GPU): null pointers, head-group mismatch, head sizes and
     block sizes outside the compiled set, bad enums, bad scale, short block
@@ -331,3 +331,27 @@ def test_fp8_prefill_workspace_size_is_arithmetic(lib):
     assert lib.attn_fp8_prefill_workspace_size(2, 200, 2, 128, 64) == 2 * 8 * 16384 * 2 + 256
     assert lib.attn_fp8_prefill_workspace_size(0, 200, 2, 128, 64) == 0
     assert lib.attn_fp8_prefill_workspace_size(1, 0, 1, 64, 16) == 2 * 1024 * 2 + 256
+
+
+def test_header_is_plain_c_and_links(lib, tmp_path):
+    """A C99 program (no C++) includes include/attn_fwd.h without a warning
+    under -Wall -Wextra -pedantic, links against the shared library and calls
+    two entry points that need no GPU."""
+    import subprocess
+    import attention_forward_sdpa_gb300 as pkg
+    src = tmp_path / "use_header.c"
+    src.write_text('#include "attn_fwd.h"\n#include <stdio.h>\n'
+                   "int main(void) {\n"
+                   '  printf("%d|%s\\n", (int)attn_abi_version(),\n'
+                   "         attn_status_string(ATTN_ERR_BAD_BLOCK_TABLE));\n"
+                   "  return attn_decode_workspace_size(2, 4, 128, 1) == 256 ? 0 : 1;\n"
+                   "}\n")
+    exe = tmp_path / "use_header"
+    libdir = os.path.dirname(pkg.library_path())
+    cc = subprocess.run(["gcc", "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror",
+                         f"-I{HEADER_DIR}", str(src), f"-L{libdir}", "-lattn_fwd_sm103",
+                         f"-Wl,-rpath,{libdir}", "-o", str(exe)], capture_output=True, text=True)
+    assert cc.returncode == 0, cc.stderr
+    run = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
+    assert run.returncode == 0, run.stderr
+    assert run.stdout.strip() == "2|block table entry out of range"
