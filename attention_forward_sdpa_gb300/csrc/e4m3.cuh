@@ -10,8 +10,14 @@
 // normal codes and for the subnormal ones (e = 0), which land on subnormals
 // of the target with the same fraction.  One multiply by 2^8 or 2^120 in the
 // target format then gives the value exactly (no rounding: a power of two,
-// no overflow; subnormal inputs are honoured by mul.rn without .ftz).  The
-// two NaN codes (S.1111.111) come out as +-480 instead of NaN.
+// no overflow; subnormal inputs are honoured by mul.rn without .ftz).
+//
+// The two NaN codes (S.1111.111) would land on +-480 that way (no finite
+// code is 480: the largest is 448), so before the multiply the lanes whose
+// placed bits are all ones get the rest of the target's exponent field set,
+// which makes them NaN (and the product NaN).  Detection without a compare:
+// adding one unit of the lowest placed bit to the masked field carries out
+// of it only when every placed bit is one.
 #pragma once
 
 #include <cstdint>
@@ -26,10 +32,18 @@ __device__ __forceinline__ uint32_t e4m3x2_widen(uint32_t w, uint32_t sel) {
   uint32_t x, r;
   asm("prmt.b32 %0, %1, 0, %2;" : "=r"(x) : "r"(w), "r"(sel));
   if constexpr (BF16) {
-    const uint32_t y = (x << 4) & 0x87F087F0u;   // s | eeee.mmm at bits 10..4: value * 2^-120
+    uint32_t y = (x << 4) & 0x87F087F0u;          // s | eeee.mmm at bits 10..4: value * 2^-120
+    // NaN codes: bits 10..4 all set -> the carry lands in bit 11; 15 * 0x0800
+    // sets bits 14..11, completing the all-ones exponent (no lane overflows)
+    const uint32_t nan = ((y & 0x07F007F0u) + 0x00100010u) & 0x08000800u;
+    y += nan * 15u;
     asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(y), "r"(0x7B807B80u));   // * 2^120
   } else {
-    const uint32_t y = (x << 7) & 0xBF80BF80u;   // s | eeee.mmm at bits 13..7: value * 2^-8
+    uint32_t y = (x << 7) & 0xBF80BF80u;          // s | eeee.mmm at bits 13..7: value * 2^-8
+    // NaN codes: bits 13..7 all set -> the carry is bit 14, the one exponent
+    // bit still clear
+    const uint32_t nan = ((y & 0x3F803F80u) + 0x00800080u) & 0x40004000u;
+    y += nan;
     asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(y), "r"(0x5C005C00u));    // * 2^8
   }
   return r;

@@ -244,7 +244,12 @@ typedef struct {
    * it; this library takes the common convention).  kv_fp8 = 1: k_cache and
    * v_cache hold OCP E4M3 codes (1 byte per element, same [num_blocks,
    * block_size, Hkv, d] layout, 16-byte aligned) and the key and value meant
-   * are k_scale * code and v_scale * code; q and out keep `dtype`.  kv_fp8 = 0
+   * are k_scale * code and v_scale * code; q and out keep `dtype`.  The two
+   * NaN codes (S.1111.111) read as NaN: a NaN key makes the outputs of the
+   * rows that see it NaN; a NaN value element makes that channel NaN in
+   * every output whose tensor-core product reads it, which includes rows of
+   * the same key tile that do not see the key and, in decode, the other KV
+   * heads folded into the same work item (0 * NaN is NaN).  kv_fp8 = 0
    * ignores the four fields below.  k_scale and v_scale must be finite and
    * > 0.  Decode reads the codes in its kernels.  Prefill first widens the
    * pages each sequence references into `workspace` (device memory of at
@@ -319,12 +324,18 @@ attn_status_t attn_fwd_decode_ex(void* out, const void* q, const void* k_cache,
  *     attn_decode_workspace_size(num_seqs, num_q_heads, head_size, num_splits)
  *     > ATTN_DECODE_NOALLOC_SCRATCH_BYTES, are rejected with
  *     ATTN_ERR_WORKSPACE before anything is launched.
- *   - The first call on each device looks up the array's device address
- *     (cudaGetSymbolAddress with that device current) and caches it; make
- *     that first call before any stream capture.
- *   - All calls on a device share the array.  Each call writes every partial
- *     it reads, so nothing needs clearing, but calls that may overlap on the
- *     device (unordered streams) race and must not be issued.
+ *   - Every call looks up the array's device address in the current context
+ *     (cudaGetSymbolAddress with the caller's device current; no address is
+ *     kept between calls, so a device reset or another context is fine).
+ *     The first call in a context may load the library's device code: make
+ *     it before any stream capture.
+ *   - All calls on a device share the array.  The only value that must start
+ *     at zero, the work counter of the tcgen05 decode kernel, is zeroed on
+ *     `stream` before each of its launches; every partial o, m and l is
+ *     written before it is read.  Calls that may overlap on the device
+ *     (unordered streams) race on the array and must not be issued.
+ *   - It takes 16-bit caches and no feature flags (attn_fwd_decode's
+ *     arguments); fp8 caches and the flags need attn_fwd_decode_ex.
  *   - Other arguments, errors and the status word: as for attn_fwd_decode.
  */
 attn_status_t attn_fwd_decode_noalloc(void* out, const void* q, const void* k_cache,

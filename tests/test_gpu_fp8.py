@@ -208,3 +208,107 @@ def test_dense_fp8(layout):
     paged, _ = run_prefill(prob)
     torch.cuda.synchronize()
     assert torch.equal(packed.view(torch.int16), paged.view(torch.int16))
+
+
+# ----------------------------------------------------------------------------
+# E4M3 NaN codes (S.1111.111) in positions the kernels read and use
+# ----------------------------------------------------------------------------
+
+def _poke(cache, prob, b, j, kvh, c, code=0x7F):
+    """Store `code` as channel c of key j (sequence b, KV head kvh)."""
+    page = int(prob.block_table[b, j // prob.block_size])
+    cache.view(torch.uint8)[page, j % prob.block_size, kvh, c] = code
+
+
+def _nan_compare(out, lse, ref, ref_lse, dtype, allowed_extra=None):
+    """NaN placement and finite values against the oracle.  Every oracle NaN
+    must be a kernel NaN.  A kernel NaN the oracle does not have must satisfy
+    `allowed_extra(row, channel)` (None: none allowed).  Elements finite on
+    both sides agree within the tolerance; so do the finite log-sum-exps."""
+    torch.cuda.synchronize()
+    got = as_rows(out)
+    gn, rn = np.isnan(got), np.isnan(ref)
+    assert rn.any(), "the poked codes must reach the oracle's output"
+    assert not (rn & ~gn).any(), np.argwhere(rn & ~gn)[:5]
+    extra = np.argwhere(gn & ~rn)
+    if allowed_extra is None:
+        assert extra.size == 0, extra[:5]
+    else:
+        bad = [tuple(e) for e in extra if not allowed_extra(int(e[0]), int(e[1]))]
+        assert not bad, bad[:5]
+    both = ~gn & ~rn
+    assert np.isfinite(got[both]).all()
+    err = float(np.max(np.abs(got[both] - ref[both])))
+    assert err <= TOL[dtype], err
+    g = lse.cpu().numpy().reshape(-1).astype(np.float64)
+    assert not (np.isnan(ref_lse) & ~np.isnan(g)).any()
+    fin = np.isfinite(ref_lse) & np.isfinite(g)
+    assert np.max(np.abs(g[fin] - ref_lse[fin])) < 2e-3
+
+
+@pytest.mark.parametrize("d,hq,hkv,splits", [(128, 32, 2, 8), (128, 32, 2, 1), (64, 6, 2, 8),
+                                             (128, 6, 2, 4)])
+def test_decode_nan_codes_exact_placement(d, hq, hkv, splits):
+    """Decode items that hold one KV head (group of 16) and the SIMT kernel's
+    shapes (group of 3): a NaN key makes its sequence's rows of that KV head
+    NaN, a NaN value element makes that channel NaN, exactly as the
+    definition does."""
+    prob = problem(120, d, hq, hkv, 16, causal=False, q_lens=[1] * 4,
+                   kv_lens=[700, 33, 1500, 250])
+    _poke(prob.k_cache, prob, b=0, j=411, kvh=1, c=3)       # a visible key
+    _poke(prob.v_cache, prob, b=2, j=1499, kvh=0, c=d - 1)  # the last visible key
+    _poke(prob.v_cache, prob, b=3, j=0, kvh=1, c=0, code=0xFF)
+    out, lse = run_decode(prob, splits)
+    _nan_compare(out, lse, *oracle_fp8(prob), prob.dtype)
+
+
+def test_decode_nan_value_reaches_the_kv_heads_of_its_item():
+    """Group of 4 folds four KV heads into one tcgen05 item: a NaN value of
+    one head also reaches, through 0 * NaN in the shared product, that
+    channel of the item's other heads (same sequence), and nothing else."""
+    hq, hkv, d = 32, 8, 128
+    prob = problem(121, d, hq, hkv, 16, causal=False, q_lens=[1] * 3, kv_lens=[900, 2049, 64])
+    _poke(prob.k_cache, prob, b=1, j=2000, kvh=5, c=9)
+    _poke(prob.v_cache, prob, b=0, j=17, kvh=2, c=77)
+    g = hq // hkv
+
+    def allowed(row, ch):        # rows are (sequence, query head)
+        b, h = divmod(row, hq)
+        return b == 0 and ch == 77 and h // g // 4 == 2 // 4
+    out, lse = run_decode(prob, 8)
+    _nan_compare(out, lse, *oracle_fp8(prob), prob.dtype, allowed)
+
+
+def test_prefill_nan_codes():
+    """Prefill: a NaN key is exact (masked scores are replaced, not
+    multiplied).  A NaN value element of key j reaches that channel in the
+    rows of the sequence that see j (the definition) and, through 0 * NaN in
+    P.V, the rows of a 128-row query tile that multiplies key j's 128-key
+    tile without seeing key j -- nothing else."""
+    hq, hkv, d = 8, 2, 128
+    prob = problem(122, d, hq, hkv, 64, q_lens=(300, 1, 129), kv_lens=(300, 513, 129))
+    _poke(prob.k_cache, prob, b=0, j=5, kvh=0, c=100)       # seen by rows 5.. of sequence 0
+    _poke(prob.k_cache, prob, b=1, j=512, kvh=1, c=0)       # the decode-like row's last key
+    jv, cv = 200, 31
+    _poke(prob.v_cache, prob, b=0, j=jv, kvh=1, c=cv, code=0xFF)
+    g = hq // hkv
+
+    def allowed(row, ch):
+        tok, h = divmod(row, hq)
+        if ch != cv or h // g != 1 or not (0 <= tok < 300):
+            return False
+        i = tok                              # sequence 0: Sq = Sk = 300, offset 0
+        # row i does not see key jv, but its query tile's key loop reaches jv's tile
+        return i < jv and (i // 128) * 128 + 127 >= (jv // 128) * 128
+    out, lse = run_prefill(prob)
+    _nan_compare(out, lse, *oracle_fp8(prob), prob.dtype, allowed)
+
+
+def test_noncausal_prefill_nan_value_exact():
+    """Non-causal: every row multiplies every key it sees and sees every key,
+    so a NaN value element gives exactly the definition's NaN channel."""
+    prob = problem(123, 128, 4, 2, 64, causal=False, q_lens=(200, 64), kv_lens=(300, 70))
+    _poke(prob.v_cache, prob, b=0, j=299, kvh=1, c=64)
+    _poke(prob.k_cache, prob, b=1, j=3, kvh=0, c=0)
+    out, lse = run_prefill(prob)
+    _nan_compare(out, lse, *oracle_fp8(prob), prob.dtype)
