@@ -1,13 +1,27 @@
-"""CUDA-graph replay through attention_forward_sdpa_gb300.graphs: the replayed
-call equals the eager call bit for bit, reads the tensors' current values at
-replay time, and long prefill stays eager."""
+"""CUDA-graph replay through attention_forward_sdpa_gb300.graphs (the graph
+heuristic of "gfx942 unified attention, from the math up" sec. 9: decode and
+short prefill are replayed, long prefill runs eagerly): the replayed result
+matches the fp64 oracle within the parity tolerance (4e-2 bf16), equals the
+eager call bit for bit, reads the tensors' current values at replay time,
+and long prefill stays eager."""
+import dataclasses
+
 import pytest
 import torch
 
 import attn_inputs
-from tests.helpers import gpu_decode, gpu_prefill, to_dev
+from tests.helpers import (TOL, as_rows, gpu_decode, gpu_prefill, max_err, oracle_run, to_dev,
+                           worst)
 
 pytestmark = pytest.mark.gpu
+
+
+def _against_oracle(out, prob):
+    torch.cuda.synchronize()
+    got = as_rows(out)
+    ref, _ = oracle_run(prob)
+    err = max_err(got, ref)
+    assert err <= TOL[prob.dtype], (err, worst(got, ref))
 
 
 def test_graphed_decode_matches_eager_and_follows_new_values():
@@ -28,12 +42,14 @@ def test_graphed_decode_matches_eager_and_follows_new_values():
     graphs.decode(*args, **kw)                 # replayed
     torch.cuda.synchronize()
     assert cache.captures == 1 and cache.replays == 1
+    _against_oracle(out, prob)
     assert torch.equal(out, gpu_decode(prob, t=t))
     # new values in the same tensors: the replay reads them
     t["q"].mul_(-1.0)
     graphs.decode(*args, **kw)
     torch.cuda.synchronize()
     assert cache.replays == 2
+    _against_oracle(out, dataclasses.replace(prob, q=prob.q.neg()))
     assert torch.equal(out, gpu_decode(prob, t=t))
 
 
@@ -52,6 +68,7 @@ def test_graphed_short_prefill_and_eager_long_prefill():
                               t["query_start_loc"], t["seq_lens"], **kw)
     torch.cuda.synchronize()
     assert cache.captures == 1 and cache.replays == 2
+    _against_oracle(out, short)
     assert torch.equal(out, gpu_prefill(short, t=t))
     long = attn_inputs.paged_problem(seed=23, q_lens=[1024], kv_lens=[1024], num_q_heads=4,
                                      num_kv_heads=2, head_size=128, block_size=64,
@@ -63,4 +80,5 @@ def test_graphed_short_prefill_and_eager_long_prefill():
                               max_seqlen_k=1024, scale=long.scale, causal=True, cache=cache)
     torch.cuda.synchronize()
     assert len(cache) == 1                     # the long prefill was not captured
+    _against_oracle(outl, long)
     assert torch.equal(outl, gpu_prefill(long, t=tl))
