@@ -361,6 +361,40 @@ int decode_prepare_and_launch(DecodeParams& p, int head_size, bool bf16, void* w
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
+int check_decode_args(const void* out, const void* q, const void* k_cache, const void* v_cache,
+                      const int32_t* block_table, int32_t block_table_stride,
+                      const int32_t* seq_lens, int32_t num_seqs, int32_t max_seqlen_k,
+                      int32_t num_q_heads, int32_t num_kv_heads, int32_t head_size,
+                      int32_t block_size, int32_t num_blocks, float scale, int32_t num_splits,
+                      int dtype, int rounding, const float* lse_out, const int32_t* status_dev,
+                      bool* empty) {
+  *empty = false;
+  if (num_seqs < 0 || max_seqlen_k < 0) return ATTN_ERR_INVALID_ARG;
+  if (num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0) return ATTN_ERR_INVALID_ARG;
+  if (dtype != ATTN_F16 && dtype != ATTN_BF16) return ATTN_ERR_INVALID_ARG;
+  if (rounding < ATTN_RTNE || rounding > ATTN_OUT_F32) return ATTN_ERR_INVALID_ARG;
+  if (!valid_scale(scale)) return ATTN_ERR_INVALID_ARG;
+  if (block_size <= 0 || num_blocks <= 0) return ATTN_ERR_INVALID_ARG;
+  if (num_splits < 1 || num_splits > 64) return ATTN_ERR_INVALID_ARG;
+  if (head_size != 64 && head_size != 128 && head_size != 256) return ATTN_ERR_UNSUPPORTED;
+  if (block_size % 16 != 0) return ATTN_ERR_UNSUPPORTED;
+  if (num_seqs == 0) {
+    *empty = true;
+    return ATTN_OK;
+  }
+  if (!out || !q || !k_cache || !v_cache || !block_table || !seq_lens) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache))
+    return ATTN_ERR_INVALID_ARG;
+  if (!aligned4(block_table) || !aligned4(seq_lens) || !aligned4(lse_out) || !aligned4(status_dev))
+    return ATTN_ERR_INVALID_ARG;
+  const int64_t pages_needed = ((int64_t)max_seqlen_k + block_size - 1) / block_size;
+  if (block_table_stride < 1 || block_table_stride < pages_needed) return ATTN_ERR_INVALID_ARG;
+  if (num_seqs > 65535 || (int64_t)num_q_heads > 65535) return ATTN_ERR_UNSUPPORTED;
+  return ATTN_OK;
+}
+
+int check_device_sm103() { return check_device(); }
+
 }  // namespace attn
 
 extern "C" {
@@ -737,26 +771,15 @@ attn_status_t attn_fwd_decode_ex(void* out, const void* q, const void* k_cache,
                                  void* stream, const attn_features_t* features) {
   Features feat;
   if (read_features(features, feat) != ATTN_OK) return ATTN_ERR_INVALID_ARG;
-  if (num_seqs < 0 || max_seqlen_k < 0) return ATTN_ERR_INVALID_ARG;
-  if (num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0) return ATTN_ERR_INVALID_ARG;
-  if (dtype != ATTN_F16 && dtype != ATTN_BF16) return ATTN_ERR_INVALID_ARG;
-  if (rounding < ATTN_RTNE || rounding > ATTN_OUT_F32) return ATTN_ERR_INVALID_ARG;
-  if (!valid_scale(scale)) return ATTN_ERR_INVALID_ARG;
-  if (block_size <= 0 || num_blocks <= 0) return ATTN_ERR_INVALID_ARG;
-  if (num_splits < 1 || num_splits > 64) return ATTN_ERR_INVALID_ARG;
-  if (head_size != 64 && head_size != 128 && head_size != 256) return ATTN_ERR_UNSUPPORTED;
-  if (block_size % 16 != 0) return ATTN_ERR_UNSUPPORTED;
-  if (num_seqs == 0) return ATTN_OK;
-  if (!out || !q || !k_cache || !v_cache || !block_table || !seq_lens) return ATTN_ERR_INVALID_ARG;
-  if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache))
-    return ATTN_ERR_INVALID_ARG;
-  if (!aligned4(block_table) || !aligned4(seq_lens) || !aligned4(lse_out) || !aligned4(status_dev))
-    return ATTN_ERR_INVALID_ARG;
-  const int64_t pages_needed = ((int64_t)max_seqlen_k + block_size - 1) / block_size;
-  if (block_table_stride < 1 || block_table_stride < pages_needed) return ATTN_ERR_INVALID_ARG;
+  bool empty = false;
+  const int chk = attn::check_decode_args(out, q, k_cache, v_cache, block_table, block_table_stride,
+                                          seq_lens, num_seqs, max_seqlen_k, num_q_heads,
+                                          num_kv_heads, head_size, block_size, num_blocks, scale,
+                                          num_splits, (int)dtype, (int)rounding, lse_out,
+                                          status_dev, &empty);
+  if (chk != ATTN_OK || empty) return (attn_status_t)chk;
   const size_t need = attn_decode_workspace_size(num_seqs, num_q_heads, head_size, num_splits);
   if (!workspace || workspace_bytes < need || !aligned16(workspace)) return ATTN_ERR_WORKSPACE;
-  if (num_seqs > 65535 || (int64_t)num_q_heads > 65535) return ATTN_ERR_UNSUPPORTED;
 
   attn_status_t st = check_device();
   if (st != ATTN_OK) return st;

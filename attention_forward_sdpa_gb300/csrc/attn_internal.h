@@ -118,6 +118,22 @@ cudaError_t launch_decode_combine(const DecodeParams& p, int head_size, bool bf1
 int decode_prepare_and_launch(DecodeParams& p, int head_size, bool bf16, void* workspace,
                               cudaStream_t stream);
 
+// The argument rules the decode entry points share: everything except the
+// workspace and the device check, in one place so that the entry points
+// accept the same inputs.  Returns an attn_status_t value; ATTN_OK with
+// *empty set means there is nothing to launch (num_seqs == 0).
+int check_decode_args(const void* out, const void* q, const void* k_cache, const void* v_cache,
+                      const int32_t* block_table, int32_t block_table_stride,
+                      const int32_t* seq_lens, int32_t num_seqs, int32_t max_seqlen_k,
+                      int32_t num_q_heads, int32_t num_kv_heads, int32_t head_size,
+                      int32_t block_size, int32_t num_blocks, float scale, int32_t num_splits,
+                      int dtype, int rounding, const float* lse_out, const int32_t* status_dev,
+                      bool* empty);
+
+// ATTN_OK when the current device is an sm_103 GPU (the only target the
+// kernels are built for), else ATTN_ERR_UNSUPPORTED or ATTN_ERR_CUDA.
+int check_device_sm103();
+
 bool encode_tiled(CUtensorMap* map, bool bf16, int rank, const cuuint64_t* dims,
                   const cuuint64_t* strides_bytes, const cuuint32_t* box, const void* base,
                   CUtensorMapSwizzle swz);
