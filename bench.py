@@ -21,6 +21,11 @@ Reported (one JSON line on rank 0):
   e2e          the same metric with host buffers: per step the host->device
                copy of the step's inputs from pinned memory, the calls, and
                the device->host copy of the outputs, all timed;
+  configs      every configuration on its own (C1 fp16 S=128 d=64, C2, C3,
+               C4a causal S=8192, C4b chunked B=4 Sq=512 Sk=8192, C5 dense
+               non-causal BSHD B=4 H=16 S=16384 in each rounding mode RTNE,
+               RTNA, RTZ): device time per call, throughput and fractions of
+               the measured peaks, clocks sampled over them;
   cpu_baseline the fp64 CPU oracle on a bounded row sample of the same
                workloads (rank 0, single-GPU runs only).
 `--impl reference` times the oracle instead (the reference arm).
@@ -363,6 +368,10 @@ def run_ours(args, rank, world, dev):
         except Exception as exc:  # reported, never fatal: the eager numbers stand
             graph = {"error": f"{type(exc).__name__}: {exc}"[:200]}
 
+    configs = None
+    if not args.no_configs:
+        configs = measure_configs(args, dev, attn, flush, peaks, peak_src)
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(pp, dp, args.cpu_seconds)
@@ -382,10 +391,137 @@ def run_ours(args, rank, world, dev):
         "clocks": clocks,
         "e2e": e2e,
         "graph": graph,
+        "configs": configs,
         "cpu_baseline": cpu,
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
+
+
+# Every configuration of the workload set, timed in the default run next to
+# the step: (label, workload, rounding mode).  The dense 16384 workload is
+# timed in each output rounding mode.
+CONFIG_SET = (
+    ("C1", "prefill_causal_fp16_s128_d64", 0),
+    ("C2", PREFILL_WL, 0),
+    ("C3", DECODE_WL, 0),
+    ("C4a", "prefill_causal_bf16_s8192", 0),
+    ("C4b", "prefill_chunked_bf16_b4", 0),
+    ("C5_rtne", "dense_bf16_bshd_s16384", 0),
+    ("C5_rtna", "dense_bf16_bshd_s16384", 1),
+    ("C5_rtz", "dense_bf16_bshd_s16384", 2),
+)
+
+
+def measure_configs(args, dev, attn, flush, peaks, peak_src):
+    """Each configuration on its own: W warm-up calls, then K calls (the
+    run's --steps, at most 20 for the dense 16384 workload), each after the
+    256 MiB L2 flush, CUDA events around each call on the launching stream;
+    mean and median device time, throughput and fractions of the measured
+    peaks (burst, and sustained for the long runs), clocks sampled over the
+    whole set.  The small fp16 case is launch-bound: its CUDA-graph replay
+    time is reported too."""
+    stream = torch.cuda.current_stream(dev)
+    res = {}
+    sampler = ClockSampler(dev.index if dev.index is not None else 0)
+    sampler.start()
+    time.sleep(0.3)
+    t0 = time.time()
+    launches = 0
+    probs = {}
+    for label, name, rnd in CONFIG_SET:
+        prob = probs.get(name)
+        if prob is None:
+            probs.clear()
+            torch.cuda.empty_cache()
+            prob = probs[name] = attn_inputs.workload(name)
+        t = device_args(prob, dev)
+        out = torch.empty_like(t["q"])
+        is_decode = prob.max_seqlen_q == 1
+        if is_decode:
+            ws = torch.empty(attn.attn_decode_workspace_size(prob.num_seqs, prob.num_q_heads,
+                                                             prob.head_size, DECODE_SPLITS),
+                             dtype=torch.uint8, device=dev)
+
+            def call(s=stream):
+                attn.attn_fwd_decode(out, t["q"], t["k_cache"], t["v_cache"], t["block_table"],
+                                     t["seq_lens"], max_seqlen_k=prob.max_seqlen_k,
+                                     scale=prob.scale, num_splits=DECODE_SPLITS, workspace=ws,
+                                     stream=s)
+            per_call = 2
+        else:
+            def call(s=stream):
+                attn.attn_fwd_prefill(out, t["q"], t["k_cache"], t["v_cache"], t["block_table"],
+                                      t["query_start_loc"], t["seq_lens"],
+                                      max_seqlen_q=prob.max_seqlen_q,
+                                      max_seqlen_k=prob.max_seqlen_k, scale=prob.scale,
+                                      causal=prob.causal, rounding=rnd, stream=s)
+            per_call = 1
+        work_est = decode_bytes(prob) if is_decode else prefill_flops(prob)
+        long_run = not is_decode and work_est > 1e11     # the 8192, chunked and dense workloads
+        n = min(args.steps, 20) if work_est > 1e12 else args.steps
+        for _ in range(args.warmup):
+            flush.zero_()
+            call()
+        torch.cuda.synchronize(dev)
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(n)]
+        for a, b in evs:
+            flush.zero_()
+            a.record(stream)
+            call()
+            b.record(stream)
+        torch.cuda.synchronize(dev)
+        launches += n * per_call
+        us = [a.elapsed_time(b) * 1e3 for a, b in evs]
+        mean_us, med_us = sum(us) / len(us), statistics.median(us)
+        entry = {"workload": name, "rounding": ("RTNE", "RTNA", "RTZ")[rnd], "calls": n,
+                 "mean_us": mean_us, "median_us": med_us}
+        if is_decode:
+            work = decode_bytes(prob)
+            entry.update({"unit": "GB/s", "value": work / mean_us / 1e3,
+                          "bytes_per_call": work,
+                          "frac_of_hbm": work / mean_us / 1e3 / peaks["hbm_gbs"]})
+        else:
+            work = prefill_flops(prob)
+            v = work / mean_us / 1e6
+            entry.update({"unit": "TFLOP/s", "value": v, "flops_per_call": work,
+                          "frac_of_bf16": v / peaks["bf16_tflops"]})
+            if long_run:
+                entry["frac_of_bf16_sustained"] = v / peaks["bf16_tflops_sustained"]
+        if label == "C1":
+            g = torch.cuda.CUDAGraph()
+            cap = torch.cuda.Stream(dev)
+            cap.wait_stream(stream)
+            with torch.cuda.graph(g, stream=cap):
+                call(cap)
+            torch.cuda.synchronize(dev)
+            gev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(n)]
+            for a, b in gev:
+                flush.zero_()
+                a.record(stream)
+                g.replay()
+                b.record(stream)
+            torch.cuda.synchronize(dev)
+            launches += n
+            entry["graph_median_us"] = statistics.median(a.elapsed_time(b) * 1e3 for a, b in gev)
+            entry["note"] = "launch-bound (no roofline claim)"
+            del g
+        res[label] = entry
+        del t, out
+    t1 = time.time()
+    sampler.stop()
+    probs.clear()
+    torch.cuda.empty_cache()
+    res["peaks"] = {"bf16_tflops": peaks["bf16_tflops"],
+                    "bf16_tflops_sustained": peaks["bf16_tflops_sustained"],
+                    "hbm_gbs": peaks["hbm_gbs"], "source": peak_src}
+    res["clocks"] = sampler.summary(t0, t1)
+    res["gpu_launches"] = launches
+    res["l2"] = "flushed before every call (256 MiB write)"
+    res["gpu"] = "this rank's GPU (rank 0 prints)"
+    return res
 
 
 def measure_graph(pp, dp, pt, dt, p_out, d_out, ws, flush, attn, dev, n=50):
@@ -803,6 +939,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="skip the CUDA-graph replay timings")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the per-configuration timings (C1-C5) of the default line")
     ap.add_argument("--cpu-seconds", type=float, default=16.0)
     ap.add_argument("--ref-rows", type=int, default=128)
     ap.add_argument("--cpu-sweep", action="store_true",
