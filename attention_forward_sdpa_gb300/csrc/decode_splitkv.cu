@@ -358,8 +358,9 @@ __global__ void __launch_bounds__(kDecWarps * 32) decode_split_kernel(const __gr
         finish_row(M, L, p.sinks[h0 + h], inv_l, lse_v);
         v = acc * inv_l;
       } else {
-        v = L > 0.f ? acc / L : 0.f;
-        lse_v = L > 0.f ? M * kLn2 + logf(L) : -INFINITY;
+        // L == 0: no visible key; a NaN L (a NaN score) stays NaN
+        v = L != 0.f ? acc / L : 0.f;
+        lse_v = L != 0.f ? M * kLn2 + logf(L) : -INFINITY;
       }
       v *= p.out_scale;   // fp8 V factor (1 otherwise)
       store_out<BF16>(p.out, row * D + e, &v, 1, p.rounding);

@@ -20,13 +20,14 @@ __device__ __forceinline__ float rewrite_score(float x, float cap, float inv_cap
   return fmaf(-slope, fabsf(dist), x);
 }
 
-// A tile row of raw scores q.k (fp32 bit patterns in s[c][e], key column
-// 32c + e): each becomes (rewrite(tau * q.k)) / tau, so that the softmax that
+// A row of raw scores q.k (fp32 bit patterns in s[c][e], key column 32c + e
+// of the NC * 32 columns passed): each becomes (rewrite(tau * q.k)) / tau, so that the softmax that
 // follows, which multiplies by tau * log2(e), sees the rewritten score.  d0 is
 // the distance from the row's aligned key to column 0 (diag - first key).
 // The constants are folded so that an element costs one multiply, one MUFU
 // tanh and one FMA: (cap / tau) * tanh(q.k * tau / cap) - (slope / tau) * |dist|.
-__device__ __forceinline__ void rewrite_scores(uint32_t (&s)[4][32], float tau, float cap,
+template <int NC>
+__device__ __forceinline__ void rewrite_scores(uint32_t (&s)[NC][32], float tau, float cap,
                                                float slope, float d0) {
   const float inv_tau = 1.f / tau;
   const float ks = -slope * inv_tau;
@@ -34,7 +35,7 @@ __device__ __forceinline__ void rewrite_scores(uint32_t (&s)[4][32], float tau, 
     const float a = tau / cap;
     const float b = cap * inv_tau;
 #pragma unroll
-    for (int c = 0; c < 4; ++c)
+    for (int c = 0; c < NC; ++c)
 #pragma unroll
       for (int e = 0; e < 32; ++e) {
         const float t = fast_tanh(__uint_as_float(s[c][e]) * a);
@@ -42,7 +43,7 @@ __device__ __forceinline__ void rewrite_scores(uint32_t (&s)[4][32], float tau, 
       }
   } else {
 #pragma unroll
-    for (int c = 0; c < 4; ++c)
+    for (int c = 0; c < NC; ++c)
 #pragma unroll
       for (int e = 0; e < 32; ++e)
         s[c][e] = __float_as_uint(fmaf(ks, fabsf(d0 - (float)(32 * c + e)), __uint_as_float(s[c][e])));
@@ -59,8 +60,10 @@ __device__ __forceinline__ void finish_row(float m, float l, float sink, float& 
   constexpr float kLn2f = 0.693147180559945309f;
   constexpr float kLog2ef = 1.4426950408889634f;
   if (sink == -INFINITY) {
-    inv_l = l > 0.f ? 1.f / l : 0.f;
-    lse = l > 0.f ? m * kLn2f + logf(l) : -INFINITY;
+    // l == 0: no visible key; a NaN l (from a NaN score) gives NaN, as the
+    // definition does
+    inv_l = l != 0.f ? 1.f / l : 0.f;
+    lse = l != 0.f ? m * kLn2f + logf(l) : -INFINITY;
     return;
   }
   const float zl = sink * kLog2ef;
