@@ -312,6 +312,7 @@ def run_ours(args, rank, world, dev):
     barrier(world)
     torch.cuda.synchronize(dev)
     t_wall0 = time.time()
+    host_gate(stream, K)
     ev_all[0].record(stream)
     for k in range(K):
         flush.zero_()
@@ -466,6 +467,7 @@ def measure_configs(args, dev, attn, flush, peaks, peak_src):
         torch.cuda.synchronize(dev)
         evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                for _ in range(n)]
+        host_gate(stream, n)
         for a, b in evs:
             flush.zero_()
             a.record(stream)
@@ -522,6 +524,16 @@ def measure_configs(args, dev, attn, flush, peaks, peak_src):
     res["l2"] = "flushed before every call (256 MiB write)"
     res["gpu"] = "this rank's GPU (rank 0 prints)"
     return res
+
+
+def host_gate(stream, calls, host_ms_per_call=0.4):
+    """Holds the stream in a device-side spin (torch.cuda._sleep) long enough
+    for the host to enqueue `calls` timed calls behind it, so that no CUDA
+    event span includes time the GPU spent waiting for the Python host to
+    issue the next launch.  The spin runs before the first timed event."""
+    cycles = int((calls * host_ms_per_call + 5.0) * 1e-3 * 2.1e9)
+    with torch.cuda.stream(stream):
+        torch.cuda._sleep(cycles)
 
 
 def measure_graph(pp, dp, pt, dt, p_out, d_out, ws, flush, attn, dev, n=50):
@@ -795,6 +807,7 @@ def pages_protocol(call, stream, dev, measurements=10, launches=50, trim=0.2):
     times = []
     for _ in range(measurements):
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        host_gate(stream, launches)
         a.record(stream)
         for _ in range(launches):
             call()
@@ -864,6 +877,7 @@ def run_sweep(args, dev):
         sampler.start()
         time.sleep(0.3)
         t0 = time.time()
+        host_gate(stream, n)
         for a, b in evs:
             flush.zero_()
             a.record(stream)
