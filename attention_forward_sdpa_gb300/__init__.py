@@ -39,6 +39,7 @@ from .build_ext import LIB_PATH
 __all__ = ["attn_fwd_prefill", "attn_fwd_dense", "attn_fwd_decode", "attn_fwd_decode_noalloc",
            "has_features", "dense",
            "attn_decode_workspace_size", "attn_fp8_prefill_workspace_size",
+           "attn_prefill_split_workspace_size",
            "attn_round_f32", "attn_status_string", "attn_abi_version", "attn_tensor_map_cache_stats",
            "prefill", "decode",
            "AttnError", "library_path", "load_library", "RTNE", "RTNA", "RTZ", "OUT_F32"]
@@ -81,6 +82,12 @@ def load_library() -> ctypes.CDLL:
         lib.attn_fwd_prefill.argtypes = [P, P, P, P, P, i32, P, P, i32, i32, i32, i32, i32, i32,
                                          i32, i32, i32, f32, i32, ctypes.c_int, ctypes.c_int, P,
                                          P, P]
+        lib.attn_fwd_prefill_split.restype = ctypes.c_int
+        lib.attn_fwd_prefill_split.argtypes = [P, P, P, P, P, i32, P, P, i32, i32, i32, i32, i32,
+                                               i32, i32, i32, i32, f32, i32, ctypes.c_int,
+                                               ctypes.c_int, P, P, P, sz, P]
+        lib.attn_prefill_split_workspace_size.restype = sz
+        lib.attn_prefill_split_workspace_size.argtypes = [i32]
         lib.attn_fwd_dense.restype = ctypes.c_int
         lib.attn_fwd_dense.argtypes = [P, P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, f32,
                                        i32, ctypes.c_int, ctypes.c_int, P, P, P]
@@ -283,8 +290,10 @@ def attn_fwd_prefill(out, q, k_cache, v_cache, block_table, query_start_loc, seq
                      max_seqlen_q: int, max_seqlen_k: int, scale: float, causal: bool,
                      rounding: int = RTNE, lse=None, status=None, stream=None, window=None,
                      softcap: float = 0.0, alibi_slopes=None, sinks=None, kv_scales=None,
-                     fp8_workspace=None) -> None:
-    """Calls attn_fwd_prefill (attn_fwd_prefill_ex with feature flags) on torch
+                     fp8_workspace=None, split_workspace=None) -> None:
+    """Calls attn_fwd_prefill (attn_fwd_prefill_ex with feature flags, or
+    attn_fwd_prefill_split when ``split_workspace`` -- a uint8 CUDA tensor of
+    attn_prefill_split_workspace_size(head_size) bytes -- is given) on torch
     CUDA tensors (shapes as in the C header)."""
     lib = load_library()
     dt = _dtype_code(q.dtype)
@@ -321,7 +330,15 @@ def attn_fwd_prefill(out, q, k_cache, v_cache, block_table, query_start_loc, seq
                 int(bool(causal)), dt, int(rounding), _ptr(lse), _ptr(status),
                 _stream_handle(stream))
         feat = _features(hq, window, softcap, alibi_slopes, sinks, kv_scales, fp8_workspace)
-        if feat is None:
+        if split_workspace is not None:
+            if feat is not None:
+                raise ValueError("the split prefill takes no feature flags")
+            _dev(split_workspace, "split_workspace", torch.uint8)
+            _same_device(q.device, split_workspace=split_workspace)
+            _check(lib.attn_fwd_prefill_split(*args[:-1], _ptr(split_workspace),
+                                              split_workspace.numel(), args[-1]),
+                   "attn_fwd_prefill_split")
+        elif feat is None:
             _check(lib.attn_fwd_prefill(*args), "attn_fwd_prefill")
         else:
             _check(lib.attn_fwd_prefill_ex(*args, ctypes.byref(feat)), "attn_fwd_prefill_ex")
@@ -485,13 +502,18 @@ def attn_round_f32(out, x, *, dtype: torch.dtype, rounding: int, stream=None) ->
 # allocating conveniences
 # ----------------------------------------------------------------------------
 
+def attn_prefill_split_workspace_size(head_size: int) -> int:
+    return int(load_library().attn_prefill_split_workspace_size(int(head_size)))
+
+
 def prefill(q, k_cache, v_cache, block_table, query_start_loc, seq_lens, *, max_seqlen_q: int,
             max_seqlen_k: int, scale: float | None = None, causal: bool = True,
             rounding: int = RTNE, return_lse: bool = False, status=None, stream=None,
-            **features):
+            split: bool = False, **features):
     """Returns O (and the log-sum-exp when asked) for a paged prefill problem.
     ``features``: window, softcap, alibi_slopes, sinks, kv_scales (see the
-    module doc); with kv_scales the fp8 workspace is allocated here."""
+    module doc); with kv_scales the fp8 workspace is allocated here.
+    ``split=True`` runs attn_fwd_prefill_split with a workspace allocated here."""
     if scale is None:
         scale = q.shape[-1] ** -0.5
     out = torch.empty(q.shape, dtype=torch.float32 if rounding == OUT_F32 else q.dtype,
@@ -503,6 +525,9 @@ def prefill(q, k_cache, v_cache, block_table, query_start_loc, seq_lens, *, max_
                                                  k_cache.shape[1])
         features = dict(features, fp8_workspace=torch.empty(max(nbytes, 1), dtype=torch.uint8,
                                                             device=q.device))
+    if split:
+        features = dict(features, split_workspace=torch.empty(
+            attn_prefill_split_workspace_size(q.shape[-1]), dtype=torch.uint8, device=q.device))
     attn_fwd_prefill(out, q, k_cache, v_cache, block_table, query_start_loc, seq_lens,
                      max_seqlen_q=max_seqlen_q, max_seqlen_k=max_seqlen_k, scale=scale,
                      causal=causal, rounding=rounding, lse=lse, status=status, stream=stream,

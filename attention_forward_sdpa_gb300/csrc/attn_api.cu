@@ -12,8 +12,10 @@
 #include <cmath>
 #include <cstdint>
 #include <atomic>
+#include <chrono>
 #include <cstring>
 #include <mutex>
+#include <random>
 
 #include "../../include/attn_fwd.h"
 #include "attn_internal.h"
@@ -52,6 +54,18 @@ attn_status_t check_device() {
 }
 
 constexpr uint64_t kDefaultWaitLimitNs = 4000000000ull;   // 4 s per pipeline wait
+
+// Call numbers that tag the split prefill's merge tickets: a process-wide
+// counter that starts at a random 48-bit value, so that tickets left in a
+// workspace by earlier calls (or by nothing: fresh memory) do not match.
+uint64_t next_call_epoch() {
+  static std::atomic<uint64_t> counter{[] {
+    std::random_device rd;
+    const uint64_t t = (uint64_t)std::chrono::steady_clock::now().time_since_epoch().count();
+    return ((uint64_t)rd() << 32 ^ (uint64_t)rd() ^ t * 0x9E3779B97F4A7C15ull) & 0xFFFFFFFFFFFFull;
+  }()};
+  return counter.fetch_add(1, std::memory_order_relaxed) + 1;
+}
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -431,7 +445,8 @@ attn_status_t prefill_impl(void* out, const void* q, const void* k_cache, const 
                            int32_t causal, attn_dtype_t dtype, attn_round_t rounding,
                            float* lse_out, int32_t* status_dev, void* stream,
                            uint64_t wait_limit_ns, int32_t stall_producer,
-                           const attn_features_t* features) {
+                           const attn_features_t* features, bool split = false,
+                           void* split_ws = nullptr, size_t split_ws_bytes = 0) {
   // ---- host-side validation (no CUDA call before this block ends)
   Features feat;
   if (read_features(features, feat) != ATTN_OK) return ATTN_ERR_INVALID_ARG;
@@ -460,6 +475,9 @@ attn_status_t prefill_impl(void* out, const void* q, const void* k_cache, const 
   int64_t gz = 0, gx = 0;
   prefill_grid(head_size, pair_heads, num_q_heads, row_blocks, gx, gz);
   if (num_seqs > 65535 || gz > 65535 || gx > 2147483647) return ATTN_ERR_UNSUPPORTED;
+  if (split && (!split_ws || split_ws_bytes < attn_prefill_split_workspace_size(head_size) ||
+                (reinterpret_cast<uintptr_t>(split_ws) & 255u)))
+    return ATTN_ERR_WORKSPACE;
 
   // fp8 caches: the K factor joins tau, the V factor scales the output
   const float scale_eff = feat.kv_fp8 ? scale * feat.k_scale : scale;
@@ -547,11 +565,60 @@ attn_status_t prefill_impl(void* out, const void* q, const void* k_cache, const 
   p.stall_producer = stall_producer;
   set_features(p, feat, scale_eff);
 
+  // The split grid: head sizes 64 / 128 without feature flags, a batch its
+  // tables hold, and more key tiles (at most) than two per SM.
+  const bool feat_on = p.win_left >= 0 || p.win_right >= 0 || p.score_xform || p.sinks ||
+                       p.out_scale != 1.f;
+  if (split && head_size != 256 && !feat_on && !stall_producer && num_seqs <= attn::kSkMaxSeqs &&
+      max_seqlen_q <= 65536) {
+    const int sms = attn::device_sm_count();
+    if (sms <= 0) return ATTN_ERR_CUDA;
+    const int64_t key_tiles = ((int64_t)max_seqlen_k + 127) / 128;
+    if ((int64_t)num_seqs * gx * gz * key_tiles >= 2 * (int64_t)sms) {
+      const int G = sms < attn::kSkMaxCtas ? sms : attn::kSkMaxCtas;
+      uint8_t* ws = static_cast<uint8_t*>(split_ws);
+      const size_t part_o_bytes = (size_t)2 * attn::kSkMaxCtas * 2 * 128 * (size_t)head_size * 4;
+      const size_t part_ml_bytes = (size_t)2 * attn::kSkMaxCtas * 2 * 128 * 2 * 4;
+      p.sk_units_x = (int32_t)gx;
+      p.sk_part_o = reinterpret_cast<float*>(ws);
+      p.sk_part_ml = reinterpret_cast<float*>(ws + part_o_bytes);
+      p.sk_ticket = reinterpret_cast<unsigned long long*>(ws + part_o_bytes + part_ml_bytes);
+      p.sk_epoch = next_call_epoch();
+      cudaError_t e = attn::launch_prefill_streamk(p, head_size, bf16, G, static_cast<cudaStream_t>(stream));
+      return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+    }
+  }
   dim3 grid((unsigned)gx, (unsigned)num_seqs, (unsigned)gz);
   cudaError_t e = attn::launch_prefill(p, head_size, bf16, grid, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 }  // namespace
+
+size_t attn_prefill_split_workspace_size(int32_t head_size) {
+  if (head_size != 64 && head_size != 128 && head_size != 256) return 0;
+  const size_t d = head_size == 256 ? 0 : (size_t)head_size;   // 256: the workspace goes unused
+  const size_t part_o = (size_t)2 * attn::kSkMaxCtas * 2 * 128 * d * 4;
+  const size_t part_ml = (size_t)2 * attn::kSkMaxCtas * 2 * 128 * 2 * 4;
+  const size_t tickets = (size_t)attn::kSkMaxCtas * 8;
+  return (part_o + part_ml + tickets + 255) / 256 * 256;
+}
+
+attn_status_t attn_fwd_prefill_split(void* out, const void* q, const void* k_cache,
+                                     const void* v_cache, const int32_t* block_table,
+                                     int32_t block_table_stride, const int32_t* query_start_loc,
+                                     const int32_t* seq_lens, int32_t num_seqs,
+                                     int32_t max_seqlen_q, int32_t max_seqlen_k, int32_t total_q,
+                                     int32_t num_q_heads, int32_t num_kv_heads, int32_t head_size,
+                                     int32_t block_size, int32_t num_blocks, float scale,
+                                     int32_t causal, attn_dtype_t dtype, attn_round_t rounding,
+                                     float* lse_out, int32_t* status_dev, void* workspace,
+                                     size_t workspace_bytes, void* stream) {
+  return prefill_impl(out, q, k_cache, v_cache, block_table, block_table_stride, query_start_loc,
+                      seq_lens, num_seqs, max_seqlen_q, max_seqlen_k, total_q, num_q_heads,
+                      num_kv_heads, head_size, block_size, num_blocks, scale, causal, dtype,
+                      rounding, lse_out, status_dev, stream, kDefaultWaitLimitNs, 0, nullptr, true,
+                      workspace, workspace_bytes);
+}
 
 attn_status_t attn_fwd_prefill(void* out, const void* q, const void* k_cache, const void* v_cache,
                                const int32_t* block_table, int32_t block_table_stride,

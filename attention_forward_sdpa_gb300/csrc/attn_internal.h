@@ -55,7 +55,20 @@ struct PrefillParams {
   const float* alibi;
   const float* sinks;
   float out_scale;      // factor on the normalised output (fp8 V factor; 1 otherwise)
+  // persistent stream-K launch (prefill_streamk.cu): head units per sequence,
+  // the workspace's partial results and tickets, and the call's epoch
+  int32_t sk_units_x;
+  float* sk_part_o;               // [2 G][2 tiles][128 rows][d] un-normalised o of unit parts
+  float* sk_part_ml;              // [2 G][2 tiles][128 rows][2] (m in log2 units, l)
+  unsigned long long* sk_ticket;  // [G] (epoch << 16 | parts counted)
+  uint64_t sk_epoch;
 };
+
+// Largest grid and batch the persistent stream-K prefill takes (its
+// workspace holds 2 parts per CTA; its shared-memory tables one entry per
+// sequence).
+constexpr int kSkMaxCtas = 160;
+constexpr int kSkMaxSeqs = 256;
 
 struct DecodeParams {
   CUtensorMap tm_q;     // Q [num_seqs, Hq, d]: dims (d, Hq, num_seqs), box (64, min(16, Hq), 1)
@@ -104,6 +117,10 @@ struct DecodeParams {
 cudaError_t launch_prefill(const PrefillParams& p, int head_size, bool bf16, dim3 grid,
                            cudaStream_t stream);
 cudaError_t launch_prefill_d256(const PrefillParams& p, bool bf16, dim3 grid, cudaStream_t stream);
+// The persistent stream-K prefill (head sizes 64 and 128, no feature flags):
+// `grid` CTAs, at most kSkMaxCtas.
+cudaError_t launch_prefill_streamk(const PrefillParams& p, int head_size, bool bf16, int grid,
+                                   cudaStream_t stream);
 cudaError_t launch_decode(const DecodeParams& p, int head_size, bool bf16, int group,
                           cudaStream_t stream);
 cudaError_t launch_decode_tc(const DecodeParams& p, int head_size, bool bf16, int grid,

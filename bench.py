@@ -414,6 +414,10 @@ CONFIG_SET = (
 )
 
 
+# configurations also timed through the split (persistent, key-range-balanced) prefill
+SPLIT_TIMED = ("C2", "C4a", "C4b", "C5_rtne")
+
+
 def measure_configs(args, dev, attn, flush, peaks, peak_src):
     """Each configuration on its own: W warm-up calls, then K calls (the
     run's --steps, at most 20 for the dense 16384 workload), each after the
@@ -421,7 +425,8 @@ def measure_configs(args, dev, attn, flush, peaks, peak_src):
     mean and median device time, throughput and fractions of the measured
     peaks (burst, and sustained for the long runs), clocks sampled over the
     whole set.  The small fp16 case is launch-bound: its CUDA-graph replay
-    time is reported too."""
+    time is reported too.  The causal, chunked and dense prefill workloads
+    are also timed through attn_fwd_prefill_split (object "split")."""
     stream = torch.cuda.current_stream(dev)
     res = {}
     sampler = ClockSampler(dev.index if dev.index is not None else 0)
@@ -430,6 +435,8 @@ def measure_configs(args, dev, attn, flush, peaks, peak_src):
     t0 = time.time()
     launches = 0
     probs = {}
+    split_ws = torch.empty(attn.attn_prefill_split_workspace_size(128), dtype=torch.uint8,
+                           device=dev)
     for label, name, rnd in CONFIG_SET:
         prob = probs.get(name)
         if prob is None:
@@ -451,12 +458,13 @@ def measure_configs(args, dev, attn, flush, peaks, peak_src):
                                      stream=s)
             per_call = 2
         else:
-            def call(s=stream):
+            def call(s=stream, split=False):
                 attn.attn_fwd_prefill(out, t["q"], t["k_cache"], t["v_cache"], t["block_table"],
                                       t["query_start_loc"], t["seq_lens"],
                                       max_seqlen_q=prob.max_seqlen_q,
                                       max_seqlen_k=prob.max_seqlen_k, scale=prob.scale,
-                                      causal=prob.causal, rounding=rnd, stream=s)
+                                      causal=prob.causal, rounding=rnd, stream=s,
+                                      split_workspace=split_ws if split else None)
             per_call = 1
         work_est = decode_bytes(prob) if is_decode else prefill_flops(prob)
         long_run = not is_decode and work_est > 1e11     # the 8192, chunked and dense workloads
@@ -491,6 +499,28 @@ def measure_configs(args, dev, attn, flush, peaks, peak_src):
                           "frac_of_bf16": v / peaks["bf16_tflops"]})
             if long_run:
                 entry["frac_of_bf16_sustained"] = v / peaks["bf16_tflops_sustained"]
+            if label in SPLIT_TIMED:
+                # the same configuration through attn_fwd_prefill_split
+                for _ in range(args.warmup):
+                    flush.zero_()
+                    call(split=True)
+                torch.cuda.synchronize(dev)
+                sev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                       for _ in range(n)]
+                host_gate(stream, n)
+                for a, b in sev:
+                    flush.zero_()
+                    a.record(stream)
+                    call(split=True)
+                    b.record(stream)
+                torch.cuda.synchronize(dev)
+                launches += n
+                sus = [a.elapsed_time(b) * 1e3 for a, b in sev]
+                smean = sum(sus) / len(sus)
+                entry["split"] = {"entry_point": "attn_fwd_prefill_split", "mean_us": smean,
+                                  "median_us": statistics.median(sus),
+                                  "value": work / smean / 1e6,
+                                  "frac_of_bf16": work / smean / 1e6 / peaks["bf16_tflops"]}
         if label == "C1":
             g = torch.cuda.CUDAGraph()
             cap = torch.cuda.Stream(dev)

@@ -110,6 +110,46 @@ attn_status_t attn_fwd_prefill(void* out, const void* q, const void* k_cache, co
                                void* stream);
 
 /*
+ * attn_fwd_prefill_split -- attn_fwd_prefill with the key range of work units
+ * split across a persistent grid, so that every SM gets the same number of
+ * key tiles whatever the row lengths: the tail KV split for the fractional
+ * last wave of MoonMath's HIP kernel (7minutos.es, "Dónde viven los datos y
+ * por qué 16x16x16"), with the parts of a split unit merged by the
+ * log-sum-exp combine of "gfx942 unified attention, from the math up",
+ * sec. 8.  A unit is two 128-row query tiles sharing a KV head; all key
+ * tiles of all units are laid end to end and cut into equal ranges, one per
+ * CTA; the CTA that finishes the last part of a cut unit merges its parts
+ * in key order.
+ *
+ *   arguments    as attn_fwd_prefill, plus:
+ *   workspace    device memory of at least
+ *                attn_prefill_split_workspace_size(head_size) bytes,
+ *                256-byte aligned, owned by the caller.  It needs no
+ *                initialisation and keeps nothing between calls that a
+ *                later call reads (each call tags its merge tickets with a
+ *                fresh call number), but calls that may run at the same
+ *                time must not share it.
+ * Results match attn_fwd_prefill within the same tolerance but are not
+ * bit-identical to it (a merged unit sums its keys in two or three parts);
+ * they are bit-identical from run to run (the merge order is fixed).  Head
+ * sizes 64 and 128 with at most 256 sequences take the split grid; other
+ * calls, and problems too small to fill the GPU, run attn_fwd_prefill's
+ * kernel and leave the workspace untouched.  Errors: as attn_fwd_prefill; a
+ * missing, short or misaligned workspace gives ATTN_ERR_WORKSPACE.
+ */
+size_t attn_prefill_split_workspace_size(int32_t head_size);
+attn_status_t attn_fwd_prefill_split(void* out, const void* q, const void* k_cache,
+                                     const void* v_cache, const int32_t* block_table,
+                                     int32_t block_table_stride, const int32_t* query_start_loc,
+                                     const int32_t* seq_lens, int32_t num_seqs,
+                                     int32_t max_seqlen_q, int32_t max_seqlen_k, int32_t total_q,
+                                     int32_t num_q_heads, int32_t num_kv_heads, int32_t head_size,
+                                     int32_t block_size, int32_t num_blocks, float scale,
+                                     int32_t causal, attn_dtype_t dtype, attn_round_t rounding,
+                                     float* lse_out, int32_t* status_dev, void* workspace,
+                                     size_t workspace_bytes, void* stream);
+
+/*
  * attn_fwd_dense -- the same forward for fixed-length batches held as strided
  * tensors, with no block table: logical shapes Q, O [batch, seqlen_q,
  * num_q_heads, head_size] and K, V [batch, seqlen_k, num_kv_heads, head_size]

@@ -115,6 +115,39 @@ def test_prefill_empty_problem_is_a_no_op(lib):
     assert lib.attn_fwd_prefill(*prefill_args(total_q=0)) == 0
 
 
+def split_args(ws=FAKE, ws_bytes=None, **over):
+    """attn_fwd_prefill_split: attn_fwd_prefill's arguments with the workspace
+    before the stream."""
+    a = prefill_args(**over)
+    return a[:-1] + [ws, ws_bytes if ws_bytes is not None else 64 << 20, a[-1]]
+
+
+def test_split_workspace_size(lib):
+    lib.attn_prefill_split_workspace_size.restype = ctypes.c_size_t
+    lib.attn_prefill_split_workspace_size.argtypes = [ctypes.c_int32]
+    n128 = lib.attn_prefill_split_workspace_size(128)
+    n64 = lib.attn_prefill_split_workspace_size(64)
+    # 2 parts per CTA x 160 CTAs x 2 tiles x 128 rows of (d + 2) fp32, plus the tickets
+    assert n128 == (2 * 160 * 2 * 128 * 130 * 4 + 160 * 8 + 255) // 256 * 256
+    assert n64 == (2 * 160 * 2 * 128 * 66 * 4 + 160 * 8 + 255) // 256 * 256
+    assert lib.attn_prefill_split_workspace_size(80) == 0
+    assert n128 % 256 == 0
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(ws=None), 4),
+    (dict(ws_bytes=1024), 4),
+    (dict(ws=ctypes.c_void_p(0x10080)), 4),           # not 256-byte aligned
+    (dict(q=None), 1),
+    (dict(d=80), 2),
+    (dict(bs=24), 2),
+    (dict(num_seqs=0), 0),
+])
+def test_split_prefill_rejects_bad_arguments(lib, over, code):
+    lib.attn_fwd_prefill_split.restype = ctypes.c_int
+    assert lib.attn_fwd_prefill_split(*split_args(**over)) == code
+
+
 def decode_args(**over):
     a = dict(out=FAKE, q=FAKE, k=FAKE, v=FAKE, bt=FAKE, bt_stride=512, sl=FAKE, num_seqs=64,
              max_k=8192, hq=32, hkv=8, d=128, bs=16, nb=100000, scale=0.088, splits=8, dtype=1,
