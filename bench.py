@@ -890,6 +890,11 @@ def run_sweep(args, dev):
                                      scale=prob.scale, num_splits=DECODE_SPLITS, workspace=ws,
                                      stream=stream, **feat)
         else:
+            if args.split and not feat:
+                feat = {"split_workspace": torch.empty(
+                    attn.attn_prefill_split_workspace_size(prob.head_size), dtype=torch.uint8,
+                    device=dev)}
+
             def call():
                 attn.attn_fwd_prefill(out, t["q"], t["k_cache"], t["v_cache"], t["block_table"],
                                       t["query_start_loc"], t["seq_lens"],
@@ -930,7 +935,9 @@ def run_sweep(args, dev):
             nominal = NOMINAL_PEAKS["bf16_tflops"]
             sustained = peaks.get("bf16_tflops_sustained")
             proto["value_trimmed"] = work / proto["trimmed_mean_us"] / 1e6
-        line = {"workload": name, "us": us, "value": value, "unit": unit,
+        line = {"workload": name, "entry_point": ("attn_fwd_prefill_split"
+                                                  if "split_workspace" in feat else None),
+                "us": us, "value": value, "unit": unit,
                 "frac": value / peak, "peak": peak, "peak_source": peak_src,
                 "frac_nominal": value / nominal, "peak_nominal": nominal,
                 "calls": n, "clocks": sampler.summary(t0, t1), "protocol": proto}
@@ -991,6 +998,9 @@ def main():
                     help="time the fp64 oracle on the host cores for every measured workload")
     ap.add_argument("--sweep", nargs="?", const="all", default=None,
                     help="time each named workload (comma-separated names, default all)")
+    ap.add_argument("--split", action="store_true",
+                    help="with --sweep: run flag-free prefill workloads through "
+                         "attn_fwd_prefill_split")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
