@@ -57,7 +57,11 @@ struct PrefillLayout {
   static constexpr int kNumBars = 2 + 2 * kStages + 2 + 2 + 2 + 1;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   // epilogue staging: 32 rows x 64 bytes per softmax warp (8 warps)
-  static constexpr int kStageOff = (kMiscOff + 16 + 127) / 128 * 128;
+  // the sequence's first kPreIds page ids, loaded by the producer warp
+  // during setup
+  static constexpr int kPreIds = 128;
+  static constexpr int kIdsOff = (kMiscOff + 16 + 15) / 16 * 16;
+  static constexpr int kStageOff = (kIdsOff + kPreIds * 4 + 127) / 128 * 128;
   static constexpr int kSmemBytes = kStageOff + 8 * 2048 + 1024;  // + slack for 1024-byte alignment
   static __device__ __forceinline__ constexpr uint32_t s_col(int t) { return t ? 128u : 0u; }
   static __device__ __forceinline__ constexpr uint32_t o_col(int t) { return t ? 256u + D : 256u; }
@@ -185,6 +189,20 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
   const int kvh = head[0] / group;
 
   // ------------------------------------------------------------ setup
+  // The producer warp fetches the sequence's first page ids now, so that the
+  // first K/V copies do not wait for a dependent read of the block table
+  // after setup; the loads overlap the barrier setup and TMEM allocation.
+  int32_t* pre_ids = reinterpret_cast<int32_t*>(smem + L::kIdsOff);
+  const int n_pre = p.dense ? 0 : min(L::kPreIds, (Sk + p.block_size - 1) / p.block_size);
+  int32_t pre[L::kPreIds / 32];
+  if (warp == 0) {
+    const int32_t* btp = p.block_table + (int64_t)b * p.bt_stride;
+#pragma unroll
+    for (int k = 0; k < L::kPreIds / 32; ++k) {
+      const int i = lane + 32 * k;
+      pre[k] = i < n_pre ? btp[i] : 0;
+    }
+  }
   if (threadIdx.x == 0) {
     for (int t = 0; t < 2; ++t) {
       mbar_init(bar_q_full + 8u * t, 1);
@@ -209,10 +227,16 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     tmem_alloc(smem_u32(tmem_slot), L::kTmemCols);
     tmem_relinquish();
   }
+  if (warp == 0) {
+#pragma unroll
+    for (int k = 0; k < L::kPreIds / 32; ++k) pre_ids[lane + 32 * k] = pre[k];
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // page id `i` of the sequence: from shared memory when it was fetched above
+  auto page_id = [&](const int32_t* btp, int i) -> int { return i < n_pre ? pre_ids[i] : btp[i]; };
 
   if (warp == 0) {
     // ---------------------------------------------------------- producer
@@ -245,7 +269,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         const CUtensorMap* tm = (i & 1) ? &p.tm_v : &p.tm_k;
         const int key0 = j * kBN;
         if (bs >= kBN) {
-          const int page = p.dense ? b : bt[key0 / bs];
+          const int page = p.dense ? b : page_id(bt, key0 / bs);
           if (page < 0 || page >= p.num_blocks) report_status(p.status, kStatusBadBlockTable);
           mbar_arrive_expect_tx(bar, L::kTileBytes);
           for (int h = 0; h < L::kHalves; ++h)
@@ -255,7 +279,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
           const int cnt = min(kBN / bs, n_pages - first);
           mbar_arrive_expect_tx(bar, (uint32_t)(cnt * L::kHalves * bs * 128));
           for (int r = 0; r < cnt; ++r) {
-            const int page = bt[first + r];
+            const int page = page_id(bt, first + r);
             if (page < 0 || page >= p.num_blocks) report_status(p.status, kStatusBadBlockTable);
             for (int h = 0; h < L::kHalves; ++h)
               tma_load_4d(dst + h * L::kHalfBytes + r * bs * 128, tm, bar, h * 64, kvh, 0, page);
