@@ -113,14 +113,18 @@ def test_bit_identical_runs_and_paging():
         assert torch.equal(outs[0], o)
 
 
-def test_gqa_equals_materialised_mha():
-    g = attn_inputs.paged_problem(seed=65, q_lens=[260], kv_lens=[300], num_q_heads=6,
-                                  num_kv_heads=2, head_size=256, block_size=64, causal=True)
-    m = attn_inputs.paged_problem(seed=65, q_lens=[260], kv_lens=[300], num_q_heads=6,
-                                  num_kv_heads=6, head_size=256, block_size=64, causal=True)
+# Odd and even groups, one to four pages per key tile: every query head reads
+# its KV head's pages, so the GQA result equals the MHA one on materialised K/V
+# bit for bit.
+@pytest.mark.parametrize("hq,bs", [(6, 64), (8, 64), (8, 16), (4, 256)])
+def test_gqa_equals_materialised_mha(hq, bs):
+    g = attn_inputs.paged_problem(seed=65, q_lens=[260, 900], kv_lens=[300, 1000], num_q_heads=hq,
+                                  num_kv_heads=2, head_size=256, block_size=bs, causal=True)
+    m = attn_inputs.paged_problem(seed=65, q_lens=[260, 900], kv_lens=[300, 1000], num_q_heads=hq,
+                                  num_kv_heads=hq, head_size=256, block_size=bs, causal=True)
     m.q = g.q.clone()
-    m.k_cache = g.k_cache.repeat_interleave(3, dim=2).contiguous()
-    m.v_cache = g.v_cache.repeat_interleave(3, dim=2).contiguous()
+    m.k_cache = g.k_cache.repeat_interleave(hq // 2, dim=2).contiguous()
+    m.v_cache = g.v_cache.repeat_interleave(hq // 2, dim=2).contiguous()
     m.block_table = g.block_table.clone()
     a, b = gpu_prefill(g), gpu_prefill(m)
     torch.cuda.synchronize()

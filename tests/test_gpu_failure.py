@@ -24,12 +24,15 @@ def _ptr(t):
     return ctypes.c_void_p(t.data_ptr())
 
 
+# Head size 256 runs its own kernel (one query tile per CTA, two score
+# buffers); its waits are bounded the same way.
+@pytest.mark.parametrize("head_size", [128, 256])
 @pytest.mark.parametrize("seqs", [2, 40])
-def test_prefill_wait_timeout_is_reported_and_device_stays_usable(seqs):
+def test_prefill_wait_timeout_is_reported_and_device_stays_usable(seqs, head_size):
     import attention_forward_sdpa_gb300 as attn
     lib = attn.load_library()
     prob = attn_inputs.paged_problem(seed=11, q_lens=[150] * seqs, kv_lens=[300] * seqs,
-                                     num_q_heads=8, num_kv_heads=2, head_size=128, block_size=64,
+                                     num_q_heads=8, num_kv_heads=2, head_size=head_size, block_size=64,
                                      dtype=torch.bfloat16, causal=True)
     t = to_dev(prob)
     out = torch.zeros_like(t["q"])
@@ -40,7 +43,7 @@ def test_prefill_wait_timeout_is_reported_and_device_stays_usable(seqs):
     rc = lib.attn_test_prefill_timeout(
         _ptr(out), _ptr(t["q"]), _ptr(t["k_cache"]), _ptr(t["v_cache"]), _ptr(t["block_table"]),
         t["block_table"].shape[1], _ptr(t["query_start_loc"]), _ptr(t["seq_lens"]), prob.num_seqs,
-        prob.max_seqlen_q, prob.max_seqlen_k, prob.total_q, 8, 2, 128, 64,
+        prob.max_seqlen_q, prob.max_seqlen_k, prob.total_q, 8, 2, head_size, 64,
         prob.k_cache.shape[0], prob.scale, 1, attn.BF16, 0, _ptr(status), 20_000_000,
         ctypes.c_void_p(stream.cuda_stream))
     assert rc == 0
