@@ -225,30 +225,42 @@ class ClockSampler:
         if self.thread is not None:
             self.thread.join(timeout=2)
 
+    @staticmethod
+    def _parse(line):
+        parts = [x.strip() for x in line.split(",")]
+        try:
+            return (float(parts[0]), float(parts[1]), parts[3:])
+        except Exception:
+            return None
+
+    def parsed(self, t0: float, t1: float):
+        """The samples taken between wall times t0 and t1, parsed."""
+        inside = [self._parse(l) for t, l in self.samples if t0 <= t <= t1]
+        return [x for x in inside if x]
+
     def summary(self, t0: float, t1: float):
-        def parse(line):
-            parts = [x.strip() for x in line.split(",")]
-            try:
-                return (float(parts[0]), float(parts[1]), parts[3:])
-            except Exception:
-                return None
-        inside = [parse(l) for t, l in self.samples if t0 <= t <= t1]
-        inside = [x for x in inside if x]
+        inside = self.parsed(t0, t1)
         window = "timed"
         if not inside:
-            inside = [x for x in (parse(l) for _, l in self.samples) if x]
+            inside = [x for x in (self._parse(l) for _, l in self.samples) if x]
             window = "whole run"
-        if not inside:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = set()
-        for _, _, flags in inside:
-            for n, v in zip(names, flags[1:5]):
-                if v.lower().startswith("active"):
-                    reasons.add(n)
-        return {"sm_mhz": statistics.median(x[0] for x in inside),
-                "sm_max_mhz": max(x[1] for x in inside), "reasons": sorted(reasons),
-                "samples": len(inside), "window": window}
+        return clock_summary(inside, window)
+
+
+def clock_summary(inside, window):
+    """Median SM clock, the highest maximum seen and every throttle reason
+    active in any of the parsed samples."""
+    if not inside:
+        return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    reasons = set()
+    for _, _, flags in inside:
+        for n, v in zip(names, flags[1:5]):
+            if v.lower().startswith("active"):
+                reasons.add(n)
+    return {"sm_mhz": statistics.median(x[0] for x in inside),
+            "sm_max_mhz": max(x[1] for x in inside), "reasons": sorted(reasons),
+            "samples": len(inside), "window": window}
 
 
 # ----------------------------------------------------------------------------
@@ -357,6 +369,7 @@ def run_ours(args, rank, world, dev):
               "algorithmic_per_launch": dbytes}
     dominant, other = (roof_d, roof_p) if d_ms_tot >= p_ms_tot else (roof_p, roof_d)
     clocks = sampler.summary(t_wall0, t_wall1)
+    step_samples = sampler.parsed(t_wall0, t_wall1)
 
     e2e = None
     if not args.no_e2e:
@@ -372,6 +385,15 @@ def run_ours(args, rank, world, dev):
     configs = None
     if not args.no_configs:
         configs = measure_configs(args, dev, attn, flush, peaks, peak_src)
+        # The step's timed region lasts a few ms, shorter than the sampling
+        # period, so the clocks reported for the run pool its samples with
+        # those of the configuration set's timed calls (same process, same
+        # kernels, right after it).
+        cfg_samples = configs.pop("_clock_samples", [])
+        if cfg_samples:
+            clocks = clock_summary(step_samples + cfg_samples,
+                                   f"timed: the step ({len(step_samples)} samples) and the "
+                                   f"configuration set ({len(cfg_samples)} samples)")
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -434,6 +456,7 @@ def measure_configs(args, dev, attn, flush, peaks, peak_src):
     time.sleep(0.3)
     t0 = time.time()
     launches = 0
+    spans = []          # wall-time spans of the timed calls (clock samples are kept from these)
     probs = {}
     split_ws = torch.empty(attn.attn_prefill_split_workspace_size(128), dtype=torch.uint8,
                            device=dev)
@@ -475,6 +498,7 @@ def measure_configs(args, dev, attn, flush, peaks, peak_src):
         torch.cuda.synchronize(dev)
         evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                for _ in range(n)]
+        ta = time.time()
         host_gate(stream, n)
         for a, b in evs:
             flush.zero_()
@@ -482,6 +506,7 @@ def measure_configs(args, dev, attn, flush, peaks, peak_src):
             call()
             b.record(stream)
         torch.cuda.synchronize(dev)
+        spans.append((ta, time.time()))
         launches += n * per_call
         us = [a.elapsed_time(b) * 1e3 for a, b in evs]
         mean_us, med_us = sum(us) / len(us), statistics.median(us)
@@ -507,6 +532,7 @@ def measure_configs(args, dev, attn, flush, peaks, peak_src):
                 torch.cuda.synchronize(dev)
                 sev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                        for _ in range(n)]
+                ta = time.time()
                 host_gate(stream, n)
                 for a, b in sev:
                     flush.zero_()
@@ -514,6 +540,7 @@ def measure_configs(args, dev, attn, flush, peaks, peak_src):
                     call(split=True)
                     b.record(stream)
                 torch.cuda.synchronize(dev)
+                spans.append((ta, time.time()))
                 launches += n
                 sus = [a.elapsed_time(b) * 1e3 for a, b in sev]
                 smean = sum(sus) / len(sus)
@@ -549,7 +576,9 @@ def measure_configs(args, dev, attn, flush, peaks, peak_src):
     res["peaks"] = {"bf16_tflops": peaks["bf16_tflops"],
                     "bf16_tflops_sustained": peaks["bf16_tflops_sustained"],
                     "hbm_gbs": peaks["hbm_gbs"], "source": peak_src}
-    res["clocks"] = sampler.summary(t0, t1)
+    timed = [x for ta, tb in spans for x in sampler.parsed(ta, tb)]
+    res["clocks"] = (clock_summary(timed, "timed calls") if timed else sampler.summary(t0, t1))
+    res["_clock_samples"] = timed
     res["gpu_launches"] = launches
     res["l2"] = "flushed before every call (256 MiB write)"
     res["gpu"] = "this rank's GPU (rank 0 prints)"
