@@ -106,3 +106,31 @@ def test_code_hash_ignores_comments_and_layout_but_not_code():
     c = "int f(int x) { return x + 2; }\n"
     assert bench.code_hash(a) == bench.code_hash(b)
     assert bench.code_hash(a) != bench.code_hash(c)
+
+
+def test_clock_samples_are_kept_from_timed_spans_and_summarised():
+    """The clock record: only samples inside the timed wall-time spans count;
+    the SM clock is their median, the maximum the highest seen, and a throttle
+    reason is reported when any sample shows it active."""
+    s = bench.ClockSampler(0)
+    # nvidia-smi lines: sm, max sm, power, active mask, hw, hw thermal, sw thermal, sw power cap
+    s.samples = [
+        (1.0, "1000, 2070, 300.0, 0x1, Not Active, Not Active, Not Active, Not Active"),   # idle, before
+        (2.0, "2070, 2070, 900.0, 0x0, Not Active, Not Active, Not Active, Not Active"),
+        (2.5, "2070, 2070, 1300.0, 0x4, Not Active, Not Active, Not Active, Active"),
+        (3.0, "2040, 2070, 1390.0, 0x4, Not Active, Not Active, Not Active, Active"),
+        (9.0, "300, 2070, 100.0, 0x1, Active, Not Active, Not Active, Not Active"),       # after
+        (9.5, "garbage line"),
+    ]
+    inside = s.parsed(1.5, 3.5)
+    assert [x[0] for x in inside] == [2070.0, 2070.0, 2040.0]
+    c = bench.clock_summary(inside, "timed")
+    assert c == {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"],
+                 "samples": 3, "window": "timed"}
+    # pooled spans, as the line's record pools the step with the configuration set
+    pooled = bench.clock_summary(s.parsed(1.5, 2.2) + s.parsed(8.5, 9.9), "two spans")
+    assert pooled["samples"] == 2 and pooled["reasons"] == ["hw_slowdown"]
+    assert pooled["sm_mhz"] == (2070.0 + 300.0) / 2
+    # no sample inside: the whole run is summarised and labelled so
+    assert s.summary(4.0, 5.0)["window"] == "whole run"
+    assert bench.clock_summary([], "timed")["samples"] == 0
