@@ -182,6 +182,12 @@ __global__ void __launch_bounds__(Lay<D, KV8>::kThreads, 1) decode_tc_kernel(con
   const int lane = threadIdx.x & 31;
   const int F = p.kv_per_item;              // KV heads per item (GH * F <= 16)
   const int KT = kRows / F;                 // keys per tile
+  // ALiBi raises the scores of the keys nearest the decode row, so walked in
+  // key order the running maxima climb on every tile of a steep head (an O
+  // rescale and a second CTA exchange each time).  With slopes each item
+  // walks its tiles from the last to the first: the first tile then sets the
+  // maxima, and the recurrence, exact in any order, rarely moves them.
+  const bool rev = p.alibi != nullptr;
   const int BPT = KT / 16;                  // 16-key boxes per tile
   const int G = p.num_q_heads / p.num_kv_heads;
   const int subs = G / GH;                  // query-head groups per KV head (1 unless G > 16)
@@ -333,12 +339,20 @@ __global__ void __launch_bounds__(Lay<D, KV8>::kThreads, 1) decode_tc_kernel(con
       const int32_t* bt = p.block_table + (int64_t)b * p.bt_stride;
       const int n_boxes = (k1 - k0 + 15) / 16;
       bool ok = true;
-      for (int cb = 0; cb < n_boxes && ok; cb += 64) {
-        int pg[2], rw[2];
-        load_ids(bt, k0, n_boxes, cb, pg, rw);
-        const int chunk_boxes = min(64, n_boxes - cb);
-        for (int rb = 0; rb < chunk_boxes && ok; rb += BPT) {
-          const int nbox = min(BPT, chunk_boxes - rb);
+      // the item's tiles in walk order (last to first with ALiBi slopes); a
+      // tile's BPT boxes never straddle a 64-box chunk of page ids
+      int loaded_cb = -1;
+      int pg[2] = {0, 0}, rw[2] = {0, 0};
+      for (int w = 0; w < n_tiles && ok; ++w) {
+        const int box0 = (rev ? n_tiles - 1 - w : w) * BPT;   // the tile's first box
+        const int cb = box0 & ~63;
+        if (cb != loaded_cb) {
+          load_ids(bt, k0, n_boxes, cb, pg, rw);
+          loaded_cb = cb;
+        }
+        {
+          const int rb = box0 - cb;
+          const int nbox = min(BPT, n_boxes - box0);
           const int set = rb >> 5;            // register holding this tile's ids
           const int j = lane - (rb & 31);     // this lane's box within the tile
           const bool mine = j >= 0 && j < nbox;
@@ -549,7 +563,7 @@ __global__ void __launch_bounds__(Lay<D, KV8>::kThreads, 1) decode_tc_kernel(con
         uint32_t sv[SW];
         tmem_ld_n<SW>(tmem + lane_off + s_col(g) + cwin, sv);
         tmem_ld_wait_n<SW>(sv);
-        const int key = e.k0 + t * KT + krow;
+        const int key = e.k0 + (rev ? n_tiles - 1 - t : t) * KT + krow;
         const bool valid = key >= e.lo && key < e.k1;
         const bool upper = SW > GH && F >= 2 && lane >= 16;
         float x[GH];

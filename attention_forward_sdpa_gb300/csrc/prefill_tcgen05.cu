@@ -185,6 +185,15 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
 #pragma unroll
   for (int t = 0; t < 2; ++t) cnt[t] = n_kv[t] > 0 ? n_kv[t] - j0 : 0;
   const int n_kv_max = max(cnt[0], cnt[1]);
+  // ALiBi raises the scores of the keys nearest the diagonal, so walked in
+  // key order the running max climbs on every tile of a steep head and O is
+  // rescaled each time.  With slopes, a CTA whose two tiles share one key
+  // range (two heads of a KV head over the same rows) walks its key tiles
+  // from the last to the first: the first tile then sets the max, and the
+  // recurrence, exact in any order, rarely rescales.  key_tile(w) is the key
+  // tile of walk step w.
+  const bool rev = FEAT && p.alibi != nullptr && p.pair_heads;
+  auto key_tile = [&](int w) -> int { return rev ? j0 + n_kv_max - 1 - w : j0 + w; };
   const int group = p.num_q_heads / p.num_kv_heads;
   const int kvh = head[0] / group;
 
@@ -260,7 +269,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
 #pragma unroll
       for (int s = 0; s < L::kStages; ++s) filled[s] = 0;
       for (int i = 0; i < 2 * n_kv_max; ++i) {
-        const int j = j0 + (i >> 1);
+        const int j = key_tile(i >> 1);
         const int s = i % L::kStages;
         const int u = i / L::kStages;
         if (u > 0 && !mbar_wait(bar_kv_empty + 8u * s, (u - 1) & 1, abort_flag, p.wait_limit_ns)) break;
@@ -346,10 +355,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       const int sv = iv % L::kStages;
       if (!mbar_wait(bar_kv_full + 8u * sv, (iv / L::kStages) & 1, abort_flag, p.wait_limit_ns)) break;
       tc_fence_after();
-      if ((j0 + j + 1) * kBN > Sk) {
+      const int jk = key_tile(j);
+      if ((jk + 1) * kBN > Sk) {
         // keys at or past kv_len in the last tile: their V rows may hold
         // anything (NaN included); P is 0 there but 0 * NaN is not, so zero them.
-        const int r0 = Sk - (j0 + j) * kBN;
+        const int r0 = Sk - jk * kBN;
         uint8_t* vt = smem + (sRing - base) + sv * L::kTileBytes;
         for (int idx = 0; idx < (kBN - r0) * L::kHalves * 8; ++idx) {
           const int chunk = idx & 7;
@@ -423,7 +433,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     float m = -INFINITY, l = 0.f;
     bool ok = true;
     for (int jr = 0; jr < t_nkv; ++jr) {
-      const int j = j0 + jr;                 // key tile
+      const int j = key_tile(jr);            // key tile
       if (!mbar_wait(bar_s_full + 8u * t, jr & 1, abort_flag, p.wait_limit_ns)) { ok = false; break; }
       tc_fence_after();
       uint32_t s[4][32];

@@ -167,7 +167,8 @@ def test_dense_features_equal_paged(layout):
 
 @pytest.mark.parametrize("splits", [1, 8])
 @pytest.mark.parametrize("kind", ("window_causal", "softcap", "alibi", "sinks", "all"))
-@pytest.mark.parametrize("d,hq,hkv", [(128, 32, 8), (128, 16, 2), (64, 6, 2), (256, 8, 2)])
+@pytest.mark.parametrize("d,hq,hkv", [(128, 32, 8), (128, 16, 2), (64, 6, 2), (64, 16, 4),
+                                      (256, 8, 2)])
 def test_decode_features(splits, kind, d, hq, hkv):
     prob = attn_inputs.paged_problem(seed=86, q_lens=[1] * 6, kv_lens=[1, 17, 0, 300, 2049, 700],
                                      num_q_heads=hq, num_kv_heads=hkv, head_size=d, block_size=16,
