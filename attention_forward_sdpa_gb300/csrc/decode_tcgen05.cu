@@ -339,70 +339,79 @@ __global__ void __launch_bounds__(Lay<D, KV8>::kThreads, 1) decode_tc_kernel(con
       const int32_t* bt = p.block_table + (int64_t)b * p.bt_stride;
       const int n_boxes = (k1 - k0 + 15) / 16;
       bool ok = true;
-      // the item's tiles in walk order (last to first with ALiBi slopes); a
-      // tile's BPT boxes never straddle a 64-box chunk of page ids
-      int loaded_cb = -1;
-      int pg[2] = {0, 0}, rw[2] = {0, 0};
-      for (int w = 0; w < n_tiles && ok; ++w) {
-        const int box0 = (rev ? n_tiles - 1 - w : w) * BPT;   // the tile's first box
-        const int cb = box0 & ~63;
-        if (cb != loaded_cb) {
-          load_ids(bt, k0, n_boxes, cb, pg, rw);
-          loaded_cb = cb;
-        }
-        {
-          const int rb = box0 - cb;
-          const int nbox = min(BPT, n_boxes - box0);
-          const int set = rb >> 5;            // register holding this tile's ids
-          const int j = lane - (rb & 31);     // this lane's box within the tile
-          const bool mine = j >= 0 && j < nbox;
-          const int page = set ? pg[1] : pg[0];
-          const int row = set ? rw[1] : rw[0];
-          for (int kind = 0; kind < 2; ++kind) {
-            if constexpr (KV8) {
-              // fp8: one box of 128 codes x 16 slots x F heads per 16 keys
-              // lands as 16F rows of 128 bytes in a staging tile
-              const uint32_t s8 = fills % kStages;
-              if (fills >= kStages &&
-                  !mbar_wait(bar_st_empty + 8u * s8, ((fills / kStages) - 1) & 1, abort_flag)) {
-                ok = false;
-                break;
-              }
-              const uint32_t bar = bar_st_full + 8u * s8;
-              if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)(nbox * F * 2048));
-              __syncwarp();
-              if (mine)
-                tma_load_4d(sStage + s8 * kStage8Bytes + j * F * 2048, kind == 0 ? &p.tm_k : &p.tm_v,
-                            bar, 0, row, kvh0, page);
-              last_fill[s8] = fills + 1;
-              ++fills;
-              continue;
-            }
-            const uint32_t s = fills % kSlots;
-            if (fills >= kSlots &&
-                !mbar_wait(bar_kv_empty + 8u * s, ((fills / kSlots) - 1) & 1, abort_flag)) {
-              ok = false;
-              break;
-            }
-            const uint32_t bar = bar_kv_full + 8u * s;
-            if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)(nbox * F * kVGroup));
+      // the K and V boxes of one tile: nbox boxes from box rb of the 64-box
+      // chunk whose page ids are in pg / rw (false when a wait ran out)
+      auto issue_tile = [&](int rb, int nbox, const int (&pg)[2], const int (&rw)[2]) -> bool {
+        const int set = rb >> 5;            // register holding this tile's ids
+        const int j = lane - (rb & 31);     // this lane's box within the tile
+        const bool mine = j >= 0 && j < nbox;
+        const int page = set ? pg[1] : pg[0];
+        const int row = set ? rw[1] : rw[0];
+        for (int kind = 0; kind < 2; ++kind) {
+          if constexpr (KV8) {
+            // fp8: one box of 128 codes x 16 slots x F heads per 16 keys
+            // lands as 16F rows of 128 bytes in a staging tile
+            const uint32_t s8 = fills % kStages;
+            if (fills >= kStages &&
+                !mbar_wait(bar_st_empty + 8u * s8, ((fills / kStages) - 1) & 1, abort_flag))
+              return false;
+            const uint32_t bar = bar_st_full + 8u * s8;
+            if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)(nbox * F * 2048));
             __syncwarp();
-            if (mine) {
-              const uint32_t slot = sRing + s * kTileBytes;
-              if (kind == 0) {
-                // K: [channel half][tile row], box j -> rows [16 F j, 16 F (j + 1))
-                const uint32_t dst = slot + j * F * 16 * 128;
-#pragma unroll
-                for (int h = 0; h < kHalves; ++h)
-                  tma_load_4d(dst + h * kHalfBytes, &p.tm_k, bar, 64 * h, row, kvh0, page);
-              } else {
-                // V: [16-row group][channel half][16 rows], both halves at once
-                tma_load_5d(slot + j * F * kVGroup, &p.tm_v, bar, 0, row, 0, kvh0, page);
-              }
-            }
-            last_fill[s] = fills + 1;
+            if (mine)
+              tma_load_4d(sStage + s8 * kStage8Bytes + j * F * 2048, kind == 0 ? &p.tm_k : &p.tm_v,
+                          bar, 0, row, kvh0, page);
+            last_fill[s8] = fills + 1;
             ++fills;
+            continue;
           }
+          const uint32_t s = fills % kSlots;
+          if (fills >= kSlots &&
+              !mbar_wait(bar_kv_empty + 8u * s, ((fills / kSlots) - 1) & 1, abort_flag))
+            return false;
+          const uint32_t bar = bar_kv_full + 8u * s;
+          if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)(nbox * F * kVGroup));
+          __syncwarp();
+          if (mine) {
+            const uint32_t slot = sRing + s * kTileBytes;
+            if (kind == 0) {
+              // K: [channel half][tile row], box j -> rows [16 F j, 16 F (j + 1))
+              const uint32_t dst = slot + j * F * 16 * 128;
+#pragma unroll
+              for (int h = 0; h < kHalves; ++h)
+                tma_load_4d(dst + h * kHalfBytes, &p.tm_k, bar, 64 * h, row, kvh0, page);
+            } else {
+              // V: [16-row group][channel half][16 rows], both halves at once
+              tma_load_5d(slot + j * F * kVGroup, &p.tm_v, bar, 0, row, 0, kvh0, page);
+            }
+          }
+          last_fill[s] = fills + 1;
+          ++fills;
+        }
+        return true;
+      };
+      if (!rev) {
+        // key order: chunk by chunk of 64 boxes, tile by tile
+        for (int cb = 0; cb < n_boxes && ok; cb += 64) {
+          int pg[2], rw[2];
+          load_ids(bt, k0, n_boxes, cb, pg, rw);
+          const int chunk_boxes = min(64, n_boxes - cb);
+          for (int rb = 0; rb < chunk_boxes && ok; rb += BPT)
+            ok = issue_tile(rb, min(BPT, chunk_boxes - rb), pg, rw);
+        }
+      } else {
+        // ALiBi: the last tile first (a tile's BPT boxes never straddle a
+        // 64-box chunk of page ids; a chunk is loaded when a tile enters it)
+        int loaded_cb = -1;
+        int pg[2] = {0, 0}, rw[2] = {0, 0};
+        for (int w = 0; w < n_tiles && ok; ++w) {
+          const int box0 = (n_tiles - 1 - w) * BPT;   // the tile's first box
+          const int cb = box0 & ~63;
+          if (cb != loaded_cb) {
+            load_ids(bt, k0, n_boxes, cb, pg, rw);
+            loaded_cb = cb;
+          }
+          ok = issue_tile(box0 - cb, min(BPT, n_boxes - box0), pg, rw);
         }
       }
       if (!ok) break;

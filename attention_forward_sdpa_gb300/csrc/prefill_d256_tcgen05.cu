@@ -137,14 +137,6 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_d256_kernel(const __grid_
   const int j0 = FEAT ? lo_first / kBN : 0;   // first key tile; tiles before it are skipped
   const int nkv = lim > lo_first ? (lim + kBN - 1) / kBN - j0 : 0;   // key tiles from j0
   const int kvh = head / (p.num_q_heads / p.num_kv_heads);
-  // ALiBi raises the scores of the keys nearest the diagonal, so walked in
-  // key order the running max climbs on every tile of a steep head and O is
-  // rescaled each time.  With slopes the CTA walks its key tiles from the
-  // last to the first: the first tile then sets the max, and the recurrence,
-  // exact in any order, rarely rescales.  key_tile(w) is the key tile of walk
-  // step w.
-  const bool rev = FEAT && p.alibi != nullptr;
-  auto key_tile = [&](int w) -> int { return rev ? j0 + nkv - 1 - w : j0 + w; };
 
   // ------------------------------------------------------------ setup
   if (threadIdx.x == 0) {
@@ -256,10 +248,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_d256_kernel(const __grid_
         }
         return true;
       };
-      for (int j = 0; ok && j < min(nkv, 2); ++j) ok = load_k(key_tile(j), 0) && load_k(key_tile(j), 1);
+      for (int j = 0; ok && j < min(nkv, 2); ++j) ok = load_k(j0 + j, 0) && load_k(j0 + j, 1);
       for (int j = 0; ok && j < nkv; ++j) {
-        ok = load_v(key_tile(j), 0) && load_v(key_tile(j), 1);
-        if (ok && j + 2 < nkv) ok = load_k(key_tile(j + 2), 0) && load_k(key_tile(j + 2), 1);
+        ok = load_v(j0 + j, 0) && load_v(j0 + j, 1);
+        if (ok && j + 2 < nkv) ok = load_k(j0 + j + 2, 0) && load_k(j0 + j + 2, 1);
       }
       // make sure no copy into this CTA's shared memory is still in flight
       for (int s = 0; s < kSlots; ++s)
@@ -325,7 +317,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_d256_kernel(const __grid_
       for (int h = 0; ok && h < 2; ++h) {
         int slot;
         if (!take(slot)) { ok = false; break; }
-        const int r0 = Sk - (key_tile(j) * kBN + 64 * h);   // rows >= r0 of this half lie past kv_len
+        const int r0 = Sk - ((j0 + j) * kBN + 64 * h);   // rows >= r0 of this half lie past kv_len
         if (r0 < 64) {
           // their V rows may hold anything (NaN included); P is 0 there but
           // 0 * NaN is not, so zero them
@@ -366,7 +358,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_d256_kernel(const __grid_
     bool ok = true;
     for (int j = 0; j < nkv; ++j) {
       const int buf = j & 1;
-      const int jk = key_tile(j);            // key tile
+      const int jk = j0 + j;                 // key tile
       const uint32_t tS = tmem + lane_off + 128u * buf;
       if (!mbar_wait(bar_s_full + 8u * buf, (j >> 1) & 1, abort_flag, p.wait_limit_ns)) { ok = false; break; }
       tc_fence_after();

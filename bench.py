@@ -74,8 +74,8 @@ CSRC = os.path.join(ROOT, "attention_forward_sdpa_gb300", "csrc")
 # edit of comments alone keeps it; the ncu summaries under profiles/ record
 # each capture).
 MEASURED_TRAFFIC = {
-    "prefill": ("prefill_tcgen05.cu", "4af85723fff0ecdb", 25.272832e6 + 2816.0),
-    "decode": ("decode_tcgen05.cu", "b45fedd384bec265", 1.130838e9 + 9.324800e6),
+    "prefill": ("prefill_tcgen05.cu", "8f6cfb695f3291b9", 25.273088e6 + 1536.0),
+    "decode": ("decode_tcgen05.cu", "444af5a310b1e892", 1.130843e9 + 8.262400e6),
 }
 
 
