@@ -260,7 +260,12 @@ attn_status_t attn_fwd_decode(void* out, const void* q, const void* k_cache, con
  *                -1: unbounded (causal calls are already bounded by diag).
  *   softcap      > 0: s becomes softcap * tanh(s / softcap); 0: off.
  *   alibi_slopes NULL, or a DEVICE fp32 array [num_q_heads]: s gains
- *                -alibi_slopes[h] * |diag - j| (after the softcap).
+ *                -alibi_slopes[h] * |diag - j| (after the softcap).  With
+ *                slopes, decode and the head-size-64/128 prefill (even
+ *                query-head groups) visit the keys from the last to the first,
+ *                so that the running maximum is set early; the result is the
+ *                same function, summed in another order, so it is not
+ *                bit-identical to a call without slopes even when they are 0.
  *   sinks        NULL, or a DEVICE fp32 array [num_q_heads]: a logit z_h that
  *                joins the softmax denominator with no value row,
  *                O = sum_j e^(s_j) V_j / (sum_j e^(s_j) + e^(z_h)); the
